@@ -1,0 +1,253 @@
+// fa_api.cu -- the C-ABI entry points of include/fa.h: argument checks, TMA
+// tensor maps, device checks and the device status word.  No entry point
+// allocates device memory; argument errors are returned before any CUDA call.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// Device status word of the library (one per device that loads the module).
+// Kernels OR kStatusTimeout into it; fa_get_last_device_status reads and
+// clears it.
+__device__ unsigned g_status_word;
+
+namespace {
+
+std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct DevState {
+  bool checked = false;
+  bool supported = false;
+  unsigned* status = nullptr;
+};
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+int check_sizes(int B, int H, int N_q, int N_kv, int d, int causal, float scale) {
+  if (B < 1 || H < 1 || N_q < 1 || N_kv < 1) return FA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+}  // namespace
+
+// Resolve the current device: must be compute capability 10.3 (sm_103a code
+// only); returns the watchdog handle for its kernels.
+int device_ctl(DevCtl* ctl) {
+  static std::mutex mu;
+  static DevState states[128];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 128) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> g(mu);
+  DevState& s = states[dev];
+  if (!s.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    s.supported = (major == 10 && minor == 3);
+    if (s.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      s.status = static_cast<unsigned*>(p);
+    }
+    s.checked = true;
+  }
+  if (!s.supported) return FA_ERR_UNSUPPORTED;
+  ctl->status = s.status;
+  ctl->timeout_ns = g_timeout_ns.load();
+  return FA_OK;
+}
+
+// 3-D map over a contiguous bf16 [BH, N, d] tensor: box 64 (d) x box_rows
+// x 1, 128-byte swizzle, out-of-range rows read as zero.
+int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+constexpr int kDefaultEmuPer32 = 0;
+constexpr float kDefaultTau = 8.0f;
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N_q,
+              int N_kv, int d, int causal, float scale, float tau, int emu_per_32, fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID;
+  int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (!(tau >= 0.f && tau <= 16.f)) return FA_ERR_INVALID;
+  if (emu_per_32 == -1) emu_per_32 = kDefaultEmuPer32;
+  if (emu_per_32 != 0 && emu_per_32 != 8 && emu_per_32 != 16) return FA_ERR_INVALID;
+  if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
+      misaligned(LSE, 4))
+    return FA_ERR_ALIGN;
+  FwdLaunch a;
+  st = device_ctl(&a.ctl);
+  if (st != FA_OK) return st;
+  const int BH = B * H;
+  if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH)) != FA_OK) return st;
+  a.o = O;
+  a.lse = LSE;
+  a.BH = BH;
+  a.N_q = N_q;
+  a.N_kv = N_kv;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.tau = tau;
+  a.emu_per_32 = emu_per_32;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = (d == 64) ? launch_fwd_d64(a) : launch_fwd_d128(a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N_q,
+           int N_kv, int d, int causal, float scale, fa_stream_t stream) {
+  return fa_fwd_ex(Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, kDefaultTau, -1, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
+  if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N_q;
+  const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
+  const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
+  return acc + delta;
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+           void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+           void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID;
+  int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
+      misaligned(dO, 16) || misaligned(dQ, 16) || misaligned(dK, 16) || misaligned(dV, 16) ||
+      misaligned(LSE, 4))
+    return FA_ERR_ALIGN;
+  const size_t need = fa_bwd_workspace_bytes(B, H, N_q, N_kv, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (misaligned(workspace, 256)) return FA_ERR_ALIGN;
+  BwdLaunch a;
+  st = device_ctl(&a.ctl);
+  if (st != FA_OK) return st;
+  const int BH = B * H;
+  if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmdO, dO, d, N_q, BH)) != FA_OK) return st;
+  const size_t rows = static_cast<size_t>(BH) * N_q;
+  a.o = O;
+  a.dO = dO;
+  a.lse = LSE;
+  a.dq = dQ;
+  a.dk = dK;
+  a.dv = dV;
+  a.dq_acc = static_cast<float*>(workspace);
+  a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                     (rows * d * sizeof(float) + 255) / 256 * 256);
+  a.BH = BH;
+  a.N_q = N_q;
+  a.N_kv = N_kv;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_bwd(a);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_get_last_device_status(fa_stream_t stream) {
+  DevCtl ctl;
+  const int st = device_ctl(&ctl);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, ctl.status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(ctl.status, 0, sizeof(unsigned), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return (v & kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+int fa_set_wait_timeout_ns(unsigned long long ns) {
+  if (ns < 1000ull || ns > 100000000000ull) return FA_ERR_INVALID;
+  g_timeout_ns.store(ns);
+  return FA_OK;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or device";
+    case FA_ERR_ALIGN: return "pointer misaligned";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,386 @@
+// fa_fwd_kernel.cuh -- forward exact attention for sm_103a.
+//
+// One CTA computes two 128-row query tiles of one (batch, head) against the
+// whole key sequence (or, causal, the keys up to its last query row):
+//
+//   warp 0       TMA producer: Q tiles once, then K_j, V_j into a ring of
+//                shared-memory slots (mbarrier full/empty pairs).
+//   warp 1       MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
+//                O_t += P_t V_j with P_t read from tensor memory, in the order
+//                S0 S1 | PV0 S0' PV1 S1' | ... so that the tensor core works
+//                on one tile while the softmax of the other runs.
+//   warps 2-5    softmax of tile 0, warps 6-9 softmax of tile 1; one thread
+//                owns one query row (one tensor-memory lane).
+//
+// The per-row recurrence is the online softmax of "FlashAttention: GPUメモリ
+// 階層を活用したアテンション最適化の分析" §6.2 in base 2 (t = scale*log2e*s),
+// with the conditional rescaling of "論文解説: FlashAttention-4 — Algorithm and
+// Kernel Pipelining Co-Design for Asymmetric Hardware Scaling"
+// (条件付きオンラインsoftmaxリスケーリング): the row keeps a reference maximum
+// m_ref and P = 2^(t - m_ref); O and l are rescaled by 2^(m_ref - m_new) only
+// when the row maximum rises more than tau above m_ref.  Normalisation by l
+// is deferred to the epilogue (§8.1 of the first page), which also writes
+// LSE = ln2 * (m_ref + log2 l).  Some of the exponentials take the FMA-pipe
+// cubic emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
+//
+// Causal masking skips every key tile that lies wholly above the diagonal;
+// only the last key tile of each query tile needs an element mask (it holds
+// both the diagonal and the N_kv tail).  Rows past N_q and keys past N_kv are
+// zero-filled by TMA and never stored / masked out.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "exp2.cuh"
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace fwd {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per tile
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kPanelBytes = 128 * 128;   // 128 rows x 128 B (64 bf16) swizzle panel
+
+template <int D>
+struct Cfg {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kTileBytes = kBM * D * 2;
+  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+  // barrier indices
+  static constexpr int kQFull = 0;                 // 2
+  static constexpr int kKVFull = 2;                // kSlots
+  static constexpr int kKVEmpty = 2 + kSlots;      // kSlots
+  static constexpr int kSFull = 2 + 2 * kSlots;    // 2
+  static constexpr int kPFull = 4 + 2 * kSlots;    // 2
+  static constexpr int kOFull = 6 + 2 * kSlots;    // 2
+  static constexpr int kNumBars = 8 + 2 * kSlots;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;   // tmem base, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + base alignment slack
+  // tensor-memory columns
+  __device__ static constexpr uint32_t col_S(int t) { return 128u * t; }
+  __device__ static constexpr uint32_t col_O(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  int BH, N_q, N_kv, causal;
+  int n_qpairs;       // ceil(N_q / 256)
+  int n_kv_tiles;     // ceil(N_kv / 128)
+  float c;            // scale * log2(e)
+  float tau;          // log2 units
+  DevCtl ctl;
+};
+
+__device__ __forceinline__ int tiles_for(const Params& p, int qbase) {
+  if (qbase >= p.N_q) return 0;
+  if (!p.causal) return p.n_kv_tiles;
+  return min(p.n_kv_tiles, qbase / kBN + 1);
+}
+
+template <int EMU>
+__device__ __forceinline__ float ex2_mix(float x, int col) {
+  if ((col & 31) < EMU) return ex2_poly3(x);
+  return ex2_hw(x);
+}
+
+template <int D, int EMU>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+           const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + C::kBarOff + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work tile: a pair of query tiles of one (batch, head).  Causal grids run
+  // the heaviest pairs (the last query rows) first.
+  int pair, bh;
+  if (p.causal) {
+    pair = p.n_qpairs - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else {
+    pair = static_cast<int>(blockIdx.x) % p.n_qpairs;
+    bh = static_cast<int>(blockIdx.x) / p.n_qpairs;
+  }
+  const int qbase0 = pair * 2 * kBM;
+  const int n_t[2] = {tiles_for(p, qbase0), tiles_for(p, qbase0 + kBM)};
+  const int n_max = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kQFull + 0), 1);
+    mbar_init(bar(C::kQFull + 1), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::kKVFull + s), 1);
+      mbar_init(bar(C::kKVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kSFull + t), 1);
+      mbar_init(bar(C::kPFull + t), 128);
+      mbar_init(bar(C::kOFull + t), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      for (int t = 0; t < 2; ++t) {
+        if (n_t[t] == 0) continue;
+        const uint32_t dst = sb + C::kQOff + t * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kQFull + t), C::kTileBytes);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_3d(dst + pn * kPanelBytes, &tmQ, bar(C::kQFull + t), pn * 64, qbase0 + t * kBM, bh);
+      }
+      const uint64_t keep = l2_policy_evict_last();
+      int slot = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < n_max; ++j) {
+        for (int kind = 0; kind < 2; ++kind) {
+          if (!mbar_wait(bar(C::kKVEmpty + slot), ph ^ 1, p.ctl, abort_flag)) goto producer_done;
+          const uint32_t dst = sb + C::kKVOff + slot * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kKVFull + slot), C::kTileBytes);
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d_hint(dst + pn * kPanelBytes, kind == 0 ? &tmK : &tmV, bar(C::kKVFull + slot),
+                             pn * 64, j * kBN, bh, keep);
+          if (++slot == C::kSlots) { slot = 0; ph ^= 1; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+      auto issue_S = [&](int t, int kslot) {
+        const uint32_t qa = sb + C::kQOff + t * C::kTileBytes;
+        const uint32_t ka = sb + C::kKVOff + kslot * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
+          mma_ss(tmem + C::col_S(t), sdesc_sw128(qa + off, 0, 1024), sdesc_sw128(ka + off, 0, 1024),
+                 idS, k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_PV = [&](int t, int vslot, bool acc) {
+        const uint32_t va = sb + C::kKVOff + vslot * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {
+          mma_ts(tmem + C::col_O(t), tmem + C::col_S(t) + 8 * k,
+                 sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if (n_t[t] > 0) ok = mbar_wait(bar(C::kQFull + t), 0, p.ctl, abort_flag);
+      int slot = 0;
+      uint32_t ph = 0;
+      auto next_slot = [&]() { if (++slot == C::kSlots) { slot = 0; ph ^= 1; } };
+      uint32_t pph[2] = {0, 0};
+      if (ok) {
+        const int sk = slot;
+        ok = mbar_wait(bar(C::kKVFull + sk), ph, p.ctl, abort_flag);
+        next_slot();
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (n_t[t] > 0) { issue_S(t, sk); tc_commit(bar(C::kSFull + t)); }
+          tc_commit(bar(C::kKVEmpty + sk));
+        }
+      }
+      for (int j = 0; j < n_max && ok; ++j) {
+        const int sv = slot;
+        ok = mbar_wait(bar(C::kKVFull + sv), ph, p.ctl, abort_flag);
+        next_slot();
+        const bool has_next = j + 1 < n_max;
+        int sk = -1;
+        if (ok && has_next) {
+          sk = slot;
+          ok = mbar_wait(bar(C::kKVFull + sk), ph, p.ctl, abort_flag);
+          next_slot();
+        }
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          ok = mbar_wait(bar(C::kPFull + t), pph[t], p.ctl, abort_flag);
+          pph[t] ^= 1;
+          if (!ok) break;
+          tc_fence_after();
+          issue_PV(t, sv, j > 0);
+          if (j + 1 < n_t[t]) {
+            issue_S(t, sk);
+            tc_commit(bar(C::kSFull + t));
+          } else {
+            tc_commit(bar(C::kOFull + t));
+          }
+        }
+        tc_commit(bar(C::kKVEmpty + sv));
+        if (has_next) tc_commit(bar(C::kKVEmpty + sk));
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int t = (warp - 2) >> 2;          // query tile of this warpgroup
+    const int rank = warp & 3;              // tensor-memory lane quarter
+    const int r_in_tile = rank * 32 + lane;
+    const int row = qbase0 + t * kBM + r_in_tile;
+    const int nt = n_t[t];
+    const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::col_S(t);
+    const uint32_t tO = tmem + lane_addr + C::col_O(t);
+    const float c = p.c;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), j & 1, p.ctl, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld_x128(tS, s);
+      if (j == nt - 1) {
+        int lim = p.N_kv - 1 - j * kBN;
+        if (p.causal) lim = min(lim, row - j * kBN);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > lim) s[i] = __float_as_uint(-INFINITY);
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(s[i]));
+      const float m_blk = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m_ref, m_blk);
+      bool resc = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m_ref = m_new;
+      } else if (m_new - m_ref > p.tau) {
+        resc = true;
+        alpha = ex2_hw(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + 32 * ch, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x32(tO + 32 * ch, o);
+        }
+      }
+      const float neg = -m_ref;
+      float sum[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float e0 = ex2_mix<EMU>(fmaf(__uint_as_float(s[2 * i]), c, neg), 2 * i);
+        const float e1 = ex2_mix<EMU>(fmaf(__uint_as_float(s[2 * i + 1]), c, neg), 2 * i + 1);
+        sum[i & 7] += e0 + e1;
+        pk[i] = pack_bf16x2(e0, e1);
+      }
+      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      tmem_st_x64(tS, pk);
+      tc_fence_before();
+      mbar_arrive(bar(C::kPFull + t));
+    }
+    // ------------------------------------------------------------- epilogue
+    bool ready = ok && nt > 0;
+    if (ready) ready = mbar_wait(bar(C::kOFull + t), 0, p.ctl, abort_flag);
+    if (__all_sync(0xffffffffu, ready)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + 32 * ch, o);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row < p.N_q) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (row < p.N_q)
+        p.lse[static_cast<size_t>(bh) * p.N_q + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int EMU>
+cudaError_t launch(const FwdLaunch& a) {
+  using C = Cfg<D>;
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.BH = a.BH;
+  p.N_q = a.N_q;
+  p.N_kv = a.N_kv;
+  p.causal = a.causal;
+  p.n_qpairs = (a.N_q + 2 * kBM - 1) / (2 * kBM);
+  p.n_kv_tiles = (a.N_kv + kBN - 1) / kBN;
+  p.c = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.tau = a.tau;
+  p.ctl = a.ctl;
+  auto kern = fwd_kernel<D, EMU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.n_qpairs) * p.BH;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_any(const FwdLaunch& a) {
+  switch (a.emu_per_32) {
+    case 0: return launch<D, 0>(a);
+    case 8: return launch<D, 8>(a);
+    case 16: return launch<D, 16>(a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fwd
+}  // namespace fa

@@ -1,0 +1,178 @@
+// fa_testing.cu -- test-only entry points of include/fa_testing.h: the
+// exponential paths, one tensor-core tile product, and the watchdog.
+#include <cuda_bf16.h>
+
+#include "exp2.cuh"
+#include "fa.h"
+#include "fa_internal.h"
+#include "fa_testing.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace testing {
+
+__global__ void exp2_kernel(const float* x, float* y, long long n, int mode) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    y[i] = mode == 1 ? ex2_poly3(x[i]) : ex2_hw(x[i]);
+}
+
+// One 128 x 128 x K product with the operand paths of the attention kernels.
+// Shared memory: A panels, B panels, two barriers, the tensor-memory base.
+constexpr int kTileThreads = 128;
+
+__global__ void __launch_bounds__(kTileThreads, 1)
+mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __nv_bfloat16* A, float* Cout, int K, int mode, DevCtl ctl) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int tile_bytes = 128 * K * 2;
+  const uint32_t sA = sb, sB = sb + tile_bytes;
+  const uint32_t bar_full = sb + 2 * tile_bytes, bar_done = bar_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 2 * tile_bytes + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 2 * tile_bytes + 20);
+  const bool b_mn = mode & 1, a_tmem = mode & 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_full, 1);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar_full, (a_tmem ? 0 : tile_bytes) + tile_bytes);
+    for (int pn = 0; pn < K / 64 && !a_tmem; ++pn)
+      tma_load_3d(sA + pn * 16384, &tmA, bar_full, pn * 64, 0, 0);
+    if (!b_mn) {
+      for (int pn = 0; pn < K / 64; ++pn) tma_load_3d(sB + pn * 16384, &tmB, bar_full, pn * 64, 0, 0);
+    } else {
+      // B is [K, 128]: two 64-column panels of K rows each
+      for (int pn = 0; pn < 2; ++pn) tma_load_3d(sB + pn * K * 128, &tmB, bar_full, pn * 64, 0, 0);
+    }
+  }
+  if (a_tmem) {
+    // Thread r writes row r of A into tensor-memory lane r, columns 128.. as
+    // packed bf16 pairs (low half = even k).
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(A + static_cast<size_t>(threadIdx.x) * K);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    for (int ch = 0; ch < K / 32; ++ch) {
+      uint32_t r[16];
+      for (int i = 0; i < 16; ++i) r[i] = arow[ch * 16 + i];
+      tmem_st_x16(tmem + lane_addr + 128 + 16 * ch, r);
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc_fence_after();
+    if (mbar_wait(bar_full, 0, ctl, abort_flag)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(128, 128, false, b_mn);
+      for (int k = 0; k < K / 16; ++k) {
+        const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, K * 128, 1024)
+                                 : sdesc_sw128(sB + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024);
+        if (a_tmem)
+          mma_ts(tmem, tmem + 128 + 8 * k, bd, idesc, k > 0);
+        else
+          mma_ss(tmem, sdesc_sw128(sA + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024), bd, idesc, k > 0);
+      }
+      tc_commit(bar_done);
+    }
+  }
+  __syncwarp();
+  if (__all_sync(0xffffffffu, mbar_wait(bar_done, 0, ctl, abort_flag))) {
+    tc_fence_after();
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    float* crow = Cout + static_cast<size_t>(threadIdx.x) * 128;
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t r[32];
+      tmem_ld_x32(tmem + lane_addr + 32 * ch, r);
+      for (int i = 0; i < 32; ++i) crow[32 * ch + i] = __uint_as_float(r[i]);
+    }
+  }
+  (void)lane;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+__global__ void wait_timeout_kernel(DevCtl ctl) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait runs out and flags it.
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, ctl, &abort_flag);
+}
+
+}  // namespace testing
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_test_exp2(const float* x, float* y, long long n, int mode, fa_stream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y)) || (mode != 0 && mode != 1)) return FA_ERR_INVALID;
+  if (n == 0) return FA_OK;
+  DevCtl ctl;
+  const int st = device_ctl(&ctl);
+  if (st != FA_OK) return st;
+  const long long blocks = (n + 255) / 256;
+  testing::exp2_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
+                         static_cast<cudaStream_t>(stream)>>>(x, y, n, mode);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode, fa_stream_t stream) {
+  if (!A || !B || !C || (K != 64 && K != 128) || mode < 0 || mode > 3) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) % 16)
+    return FA_ERR_ALIGN;
+  DevCtl ctl;
+  int st = device_ctl(&ctl);
+  if (st != FA_OK) return st;
+  CUtensorMap tmA, tmB;
+  if ((st = make_map_bf16(&tmA, A, K, 128, 1)) != FA_OK) return st;
+  if (mode & 1)
+    st = make_map_bf16(&tmB, B, 128, K, 1, K);   // [K, 128]: panels of 64 columns, K rows
+  else
+    st = make_map_bf16(&tmB, B, K, 128, 1);
+  if (st != FA_OK) return st;
+  const int smem = 2 * 128 * K * 2 + 64 + 1024;
+  auto kern = testing::mma_tile_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  kern<<<1, testing::kTileThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      tmA, tmB, static_cast<const __nv_bfloat16*>(A), C, K, mode, ctl);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_test_wait_timeout(unsigned long long timeout_ns, fa_stream_t stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return FA_ERR_INVALID;
+  DevCtl ctl;
+  const int st = device_ctl(&ctl);
+  if (st != FA_OK) return st;
+  ctl.timeout_ns = timeout_ns;
+  testing::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctl);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

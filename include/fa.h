@@ -1,0 +1,132 @@
+/*
+ * fa.h -- exact scaled-dot-product attention on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (forward):
+ *     S   = scale * Q K^T                     (N_q x N_kv per batch and head)
+ *     P   = softmax(S) row by row, restricted to the allowed keys
+ *     O   = P V
+ *     LSE = log(sum over allowed keys of exp(S))      (natural log)
+ * as defined in "FlashAttention: GPUメモリ階層を活用したアテンション最適化の分析"
+ * §2.1 (standard attention) and §6.1 (safe softmax), computed tile by tile
+ * with the online softmax of §6.2 so that S and P never reach HBM.  The
+ * causal mask is the lower-triangular mask of §11.3, top-left aligned: query
+ * i may attend key j iff j <= i (for N_q != N_kv as well).
+ *
+ * The backward pass returns dQ, dK, dV for a given dO, recomputing P from
+ * the saved LSE (§7.2 of the same page); it is the exact gradient of
+ * <dO, O>.  Its workspace holds D = rowsum(dO * O) and an fp32 dQ
+ * accumulator.
+ *
+ * Layout: every tensor is contiguous row-major [B, H, N, d] with d innermost
+ * (the (batch, heads, seq, head_dim) order of §11.1); LSE and D are [B, H, N_q].
+ * Element types: Q, K, V, O, dO, dQ, dK, dV bf16; LSE fp32.
+ *
+ * Ownership: all pointers are DEVICE pointers owned by the caller.  The
+ * library never frees or keeps them; calls are asynchronous on `stream`
+ * (0 = the legacy default stream) and write only the named outputs (and, for
+ * fa_bwd, the caller's workspace).
+ *
+ * Errors: every entry point returns an fa_status.  Argument checks happen on
+ * the host before anything is launched; a rejected call launches nothing and
+ * leaves all buffers untouched.  A launch failure returns FA_ERR_CUDA.  Every
+ * wait inside the kernels is bounded in time; a wait that runs out sets a
+ * device status word that fa_get_last_device_status() reports as
+ * FA_ERR_TIMEOUT (the outputs of that call are then undefined).  Nothing
+ * aborts, exits or throws across this interface.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,      /* null pointer, size < 1, causal not 0/1, bad scale */
+  FA_ERR_UNSUPPORTED = 2,  /* head dimension d not in {64, 128}; no sm_103 device */
+  FA_ERR_ALIGN = 3,        /* a pointer not 16-byte aligned (TMA requirement) */
+  FA_ERR_WORKSPACE = 4,    /* fa_bwd workspace null or smaller than required */
+  FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_TIMEOUT = 6       /* a bounded in-kernel wait ran out (device status) */
+} fa_status;
+
+/* Opaque CUDA stream (cudaStream_t); 0 selects the legacy default stream. */
+typedef void* fa_stream_t;
+
+/*
+ * fa_fwd -- forward attention.
+ *   Q   bf16 [B, H, N_q,  d]      K, V bf16 [B, H, N_kv, d]
+ *   O   bf16 [B, H, N_q,  d]      (output; fully overwritten, never read)
+ *   LSE fp32 [B, H, N_q]          (output; natural-log logsumexp of scale*QK^T)
+ *   B, H, N_q, N_kv >= 1; d in {64, 128}; causal in {0, 1};
+ *   scale finite and > 0 (typically 1/sqrt(d)).
+ * Returns FA_OK once the kernel is enqueued on `stream`.
+ */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+           int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+           fa_stream_t stream);
+
+/*
+ * fa_fwd_ex -- fa_fwd with the two exact-attention tuning knobs exposed.
+ *   tau      conditional-rescaling threshold in log2 units ("論文解説:
+ *            FlashAttention-4 ...", 条件付きオンラインsoftmaxリスケーリング):
+ *            O and l are rescaled only when a row maximum rises by more than
+ *            tau; 0 rescales on every rise.  Must be in [0, 16].  fa_fwd uses 8.
+ *   emu_per_32  how many of every 32 exponentials take the FMA-pipe cubic
+ *            2^x emulation (same page, ソフトウェア指数関数エミュレーション)
+ *            instead of the hardware ex2 unit: one of 0, 8, 16, -1 (-1 = the
+ *            library default, which fa_fwd uses).
+ * The result is exact attention for every setting, up to rounding.
+ */
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
+              int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+              float tau, int emu_per_32, fa_stream_t stream);
+
+/*
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for this
+ * problem: an fp32 dQ accumulator [B, H, N_q, d] and D = rowsum(dO * O)
+ * [B, H, N_q] fp32, each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
+
+/*
+ * fa_bwd -- backward attention.
+ *   Q, K, V, O, dO bf16 as in fa_fwd; LSE fp32 [B, H, N_q] from fa_fwd on the
+ *   same inputs.  dQ bf16 [B, H, N_q, d], dK, dV bf16 [B, H, N_kv, d]
+ *   (outputs; fully overwritten).  workspace: device memory of at least
+ *   fa_bwd_workspace_bytes(...) bytes, 256-byte aligned, owned by the caller;
+ *   its contents on entry are ignored (it is cleared inside the call).
+ * Same size, d, causal and scale rules as fa_fwd.
+ */
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+           const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+           int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+           void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_get_last_device_status -- synchronise `stream`, then read and clear the
+ * device status word of the current device.  Returns FA_OK, FA_ERR_TIMEOUT if
+ * a bounded wait in any kernel of this library ran out since the last call,
+ * or FA_ERR_CUDA if the synchronisation itself failed.
+ */
+int fa_get_last_device_status(fa_stream_t stream);
+
+/*
+ * fa_set_wait_timeout_ns -- time limit of every in-kernel wait, in
+ * nanoseconds, for launches made after this call (process-wide; default
+ * 1e9 = 1 s).  Values outside [1e3, 1e11] return FA_ERR_INVALID.
+ */
+int fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* fa_status_string -- a static, NUL-terminated description of a status code. */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

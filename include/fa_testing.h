@@ -1,0 +1,62 @@
+/*
+ * fa_testing.h -- test-only entry points of the GB300 attention library.
+ *
+ * These expose, one at a time, the device building blocks the attention
+ * kernels are made of, so that tests can check each against the CPU:
+ *   - the two ways the kernels take 2^x (hardware ex2 and the FMA-pipe cubic
+ *     emulation of "論文解説: FlashAttention-4 — Algorithm and Kernel
+ *     Pipelining Co-Design for Asymmetric Hardware Scaling",
+ *     ソフトウェア指数関数エミュレーション);
+ *   - one TMA-loaded, tcgen05 tensor-core tile product with the operand
+ *     layouts the attention kernels use;
+ *   - the bounded-wait watchdog.
+ * All pointers are caller-owned DEVICE pointers; calls are asynchronous on
+ * `stream`; the return value is an fa_status (see fa.h).
+ */
+#ifndef FA_GB300_TESTING_H
+#define FA_GB300_TESTING_H
+
+#include "fa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * fa_test_exp2 -- y[i] = 2^x[i] for i < n (fp32 in, fp32 out).
+ *   mode 0: the hardware ex2 unit (approximate, flush-to-zero).
+ *   mode 1: the cubic emulation: n = floor(x), f = x - n,
+ *           p(f) = 1 + 0.6951 f + 0.2276 f^2 + 0.0771 f^3, exponent n added
+ *           to p's exponent field by an integer operation; inputs below -127
+ *           are clamped to -127.
+ *   n >= 0 (0 launches nothing); x, y 4-byte aligned.
+ */
+int fa_test_exp2(const float* x, float* y, long long n, int mode, fa_stream_t stream);
+
+/*
+ * fa_test_mma_tile -- C = A * B^T for one tile on the tensor cores.
+ *   A bf16 [128, K] row-major (K contiguous), K in {64, 128}.
+ *   mode bit 0 clear: B bf16 [128, K] row-major (the S = Q K^T form: both
+ *                     operands K-major);
+ *   mode bit 0 set:   B bf16 [K, 128] row-major, i.e. C = A * B with the
+ *                     B operand N-major (the O += P V form);
+ *   mode bit 1 set:   A is first copied into tensor memory and the product
+ *                     reads it from there (the P operand's path);
+ *   C fp32 [128, 128] row-major (output).
+ */
+int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode,
+                     fa_stream_t stream);
+
+/*
+ * fa_test_wait_timeout -- launch one CTA that waits on a barrier nothing
+ * will ever arrive on, with a limit of timeout_ns; the wait runs out and the
+ * kernel sets the device status to FA_ERR_TIMEOUT and returns.  Used to
+ * check the watchdog path without faulting or hanging the GPU.
+ */
+int fa_test_wait_timeout(unsigned long long timeout_ns, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_TESTING_H */

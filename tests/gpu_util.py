@@ -1,0 +1,79 @@
+"""Helpers shared by the GPU parity tests (device tensors, guard bands, metrics).
+
+The tolerances are the ones fixed for this library: O max-abs error <= 1e-2
+and relative RMS <= 5e-3, LSE max-abs error <= 1e-3, dQ/dK/dV relative RMS
+<= 1e-2, emulated 2^x max relative error <= 2e-4.  Relative RMS is
+||x - ref||_2 / ||ref||_2 over the compared elements.
+"""
+import numpy as np
+
+import fa_inputs
+from oracle import attention as orc
+
+O_MAX_ABS = 1e-2
+O_REL_RMS = 5e-3
+LSE_MAX_ABS = 1e-3
+GRAD_REL_RMS = 1e-2
+GUARD = 64            # elements of guard band on each side (128 B, keeps 16 B alignment)
+
+
+def torch():
+    import torch as t
+    return t
+
+
+def dev_bf16(bits):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(t.bfloat16)
+
+
+class Guarded:
+    """A device buffer with NaN-filled guard bands around the usable view."""
+
+    def __init__(self, shape, dtype):
+        t = torch()
+        n = int(np.prod(shape))
+        self.raw = t.empty(n + 2 * GUARD, dtype=dtype, device="cuda")
+        self.raw.view(t.int16 if dtype == t.bfloat16 else t.int32).fill_(-1)   # NaN bit patterns
+        self.view = self.raw[GUARD:GUARD + n].view(shape)
+
+    def guards_intact(self):
+        t = torch()
+        w = t.int16 if self.raw.dtype == t.bfloat16 else t.int32
+        g = t.cat([self.raw[:GUARD], self.raw[-GUARD:]]).view(w)
+        return bool((g == -1).all().item())
+
+
+def to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel_rms(x, ref):
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
+
+
+def assert_o_lse(o, lse, o_ref, lse_ref, what=""):
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    assert np.all(np.isfinite(lse)), f"{what}: non-finite LSE"
+    e_max = float(np.max(np.abs(o - o_ref)))
+    e_rms = rel_rms(o, o_ref)
+    e_lse = float(np.max(np.abs(lse - lse_ref)))
+    assert e_max <= O_MAX_ABS, f"{what}: O max-abs {e_max:.3e}"
+    assert e_rms <= O_REL_RMS, f"{what}: O rel-RMS {e_rms:.3e}"
+    assert e_lse <= LSE_MAX_ABS, f"{what}: LSE max-abs {e_lse:.3e}"
+    return e_max, e_rms, e_lse
+
+
+def sample_rows(n, k, rng):
+    """Rows to compare at full size: the first and last rows, tile edges, random rows."""
+    fixed = {0, 1, n - 1, n - 2, min(127, n - 1), min(128, n - 1), min(255, n - 1), min(256, n - 1)}
+    rnd = set(rng.choice(n, size=min(n, k), replace=False).tolist())
+    return np.array(sorted(fixed | rnd))
+
+
+def oracle_rows(qb, kb, vb, b, h, rows, causal, scale):
+    q = fa_inputs.bf16_bits_to_f64(qb[b, h][rows])
+    k = fa_inputs.bf16_bits_to_f64(kb[b, h])
+    v = fa_inputs.bf16_bits_to_f64(vb[b, h])
+    return orc.head_forward(q, k, v, causal=causal, scale=scale, rows=rows)

@@ -1,0 +1,127 @@
+"""Forward parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small and ragged problems are compared element by element over the whole
+output; the full-size workloads run at their real sizes (the launch the bench
+times) and are compared on sampled (batch, head, row) outputs that the oracle
+computes one row at a time.  Every call also checks that nothing outside O
+and LSE was written (guard bands), that every output element was written
+(outputs start as NaN), and that no in-kernel wait ran out.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import exact_attention_74_gb300 as fa
+import fa_inputs
+import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    assert torch.cuda.is_available()
+    fa.library()
+    return torch
+
+
+def run_fwd(torch, qb, kb, vb, causal, scale, tau=None, emu=None):
+    B, H, N_q, d = qb.shape
+    N_kv = kb.shape[2]
+    q, k, v = gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vb)
+    o = gu.Guarded((B, H, N_q, d), torch.bfloat16)
+    lse = gu.Guarded((B, H, N_q), torch.float32)
+    if tau is None and emu is None:
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.view.data_ptr(), lse.view.data_ptr(),
+                       B, H, N_q, N_kv, d, int(causal), scale, 0)
+    else:
+        st = fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.view.data_ptr(),
+                          lse.view.data_ptr(), B, H, N_q, N_kv, d, int(causal), scale,
+                          8.0 if tau is None else tau, -1 if emu is None else emu, 0)
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    assert o.guards_intact() and lse.guards_intact()
+    return gu.to_f64(o.view), lse.view.cpu().numpy().astype(np.float64)
+
+
+def full_compare(torch, w, **kw):
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale, **kw)
+    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, causal=w.causal, scale=w.scale)
+    return gu.assert_o_lse(o, lse, o_ref, lse_ref, w.name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_d64(torch, causal):
+    full_compare(torch, fa_inputs.WORKLOADS["tiny_causal" if causal else "tiny"])
+
+
+def _wl(B, H, N_q, N_kv, d, causal, seed=7, kind="iid"):
+    return fa_inputs.Workload(f"B{B}H{H}q{N_q}kv{N_kv}d{d}c{int(causal)}", B, H, N_q, N_kv, d,
+                              causal, 1.0 / math.sqrt(d), seed, kind)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 3, 17, 128, 129, 255, 256, 257, 384, 1000])
+def test_ragged_square(torch, d, causal, n):
+    full_compare(torch, _wl(1, 2, n, n, d, causal, seed=n))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nkv", [(100, 300), (300, 100), (1, 513), (513, 1), (640, 130)])
+def test_ragged_rectangular(torch, d, causal, nq, nkv):
+    full_compare(torch, _wl(2, 1, nq, nkv, d, causal, seed=nq + nkv))
+
+
+@pytest.mark.parametrize("emu", [0, 8, 16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_exp_emulation_mix(torch, emu, d, causal):
+    full_compare(torch, _wl(1, 2, 700, 700, d, causal, seed=emu + d), emu=emu)
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
+@pytest.mark.parametrize("emu", [0, 16])
+def test_rescale_threshold_on_stress_inputs(torch, tau, emu):
+    w = fa_inputs.WORKLOADS["stress_8k"].with_(B=1, H=2, N_q=1024, N_kv=1024)
+    full_compare(torch, w, tau=tau, emu=emu)
+
+
+def test_outlier_distribution(torch):
+    w = _wl(1, 4, 1024, 1024, 128, False, seed=31, kind="outlier")
+    full_compare(torch, w)
+
+
+def sampled_compare(torch, w, heads, nrows, **kw):
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale, **kw)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    rng = np.random.default_rng(w.seed + 99)
+    for b, h in heads:
+        rows = gu.sample_rows(w.N_q, nrows, rng)
+        o_ref, lse_ref = gu.oracle_rows(qb, kb, vb, b, h, rows, w.causal, w.scale)
+        gu.assert_o_lse(o[b, h][rows], lse[b, h][rows], o_ref, lse_ref, f"{w.name} b{b} h{h}")
+
+
+@pytest.mark.parametrize("name", ["fwd_4k", "fwd_4k_causal"])
+def test_full_size_4k(torch, name):
+    w = fa_inputs.WORKLOADS[name]
+    sampled_compare(torch, w, [(0, 0), (1, 7), (3, 15)], 96)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("idx", range(6))
+def test_sequence_sweep(torch, causal, idx):
+    w = fa_inputs.sweep_workloads(causal)[idx]
+    sampled_compare(torch, w, [(0, 0), (w.B - 1, 15)], 48)
+
+
+def test_stress_full_size(torch):
+    w = fa_inputs.WORKLOADS["stress_8k"]
+    sampled_compare(torch, w, [(0, 0), (1, 9)], 64)

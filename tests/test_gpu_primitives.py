@@ -1,0 +1,94 @@
+"""Device building blocks on the GPU, each against the CPU.
+
+* both 2^x paths on a dense grid: the FMA-pipe cubic within 2e-4 of exact
+  2^x (the bound fixed for the emulation) and within fp32 rounding of the
+  oracle's float64 restatement of the same steps;
+* one TMA-loaded tcgen05 tile product in each operand form the attention
+  kernels use (both operands K-major; B N-major; A from tensor memory);
+* the watchdog: a wait that nothing satisfies runs out, the status reads
+  FA_ERR_TIMEOUT, and the context keeps working.
+"""
+import numpy as np
+import pytest
+
+import exact_attention_74_gb300 as fa
+import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    assert torch.cuda.is_available()
+    fa.library()
+    return torch
+
+
+def _exp2(torch, x, mode):
+    xd = torch.from_numpy(x.astype(np.float32)).cuda()
+    yd = torch.empty_like(xd)
+    assert fa.fa_test_exp2(xd.data_ptr(), yd.data_ptr(), xd.numel(), mode, 0) == fa.FA_OK
+    torch.cuda.synchronize()
+    return yd.cpu().numpy().astype(np.float64)
+
+
+def test_exp2_emulation_error_bound(torch):
+    x = np.concatenate([np.linspace(-126.0, 8.0, 2_000_001),
+                        np.linspace(-1.0, 1.0, 400_001),
+                        np.arange(-126, 9, dtype=np.float64)]).astype(np.float32).astype(np.float64)
+    y = _exp2(torch, x, 1)
+    rel = np.abs(y / np.exp2(x) - 1.0)
+    assert rel.max() <= 2e-4, rel.max()
+    # the same steps in float64 (oracle): agreement up to fp32 rounding
+    ref = oracle.exp2_cubic(x)
+    assert np.max(np.abs(y / ref - 1.0)) <= 2e-6
+    # exact powers of two at integers
+    ints = np.arange(-126, 9, dtype=np.float64)
+    assert np.array_equal(_exp2(torch, ints, 1), np.exp2(ints))
+
+
+def test_exp2_hardware_unit(torch):
+    x = np.linspace(-126.0, 8.0, 1_000_001).astype(np.float32).astype(np.float64)
+    y = _exp2(torch, x, 0)
+    assert np.max(np.abs(y / np.exp2(x) - 1.0)) <= 1e-6
+
+
+def test_exp2_masked_input_is_negligible(torch):
+    y = _exp2(torch, np.array([-np.inf, -1e30, -200.0]), 1)
+    assert np.all(y <= 2.0 ** -125)
+    y = _exp2(torch, np.array([-np.inf]), 0)
+    assert y[0] == 0.0
+
+
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_mma_tile(torch, K, mode):
+    rng = np.random.default_rng(1000 + K + mode)
+    a_bits = fa_inputs_bits(rng, (128, K))
+    b_shape = (K, 128) if mode & 1 else (128, K)
+    b_bits = fa_inputs_bits(rng, b_shape)
+    A, B = gu.dev_bf16(a_bits), gu.dev_bf16(b_bits)
+    C = torch.full((128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert fa.fa_test_mma_tile(A.data_ptr(), B.data_ptr(), C.data_ptr(), K, mode, 0) == fa.FA_OK
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    a = gu.fa_inputs.bf16_bits_to_f64(a_bits)
+    b = gu.fa_inputs.bf16_bits_to_f64(b_bits)
+    ref = a @ b if mode & 1 else a @ b.T
+    got = C.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-5
+
+
+def fa_inputs_bits(rng, shape):
+    return gu.fa_inputs.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+
+
+def test_watchdog_times_out_without_hanging(torch):
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    assert fa.fa_test_wait_timeout(20_000_000, 0) == fa.FA_OK      # 20 ms
+    assert fa.fa_get_last_device_status(0) == fa.FA_ERR_TIMEOUT
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK            # read clears it
+    # the context is still usable
+    x = torch.ones(16, device="cuda")
+    assert float((x * 2).sum().item()) == 32.0
