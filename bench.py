@@ -1,0 +1,424 @@
+"""Benchmark of the exact-attention hot path on one GB300 (or N, one process each).
+
+A step is one pass of the whole path over one batch of synthetic input:
+fa_fwd, then fa_bwd on the forward's O and LSE (the backward's three kernels:
+D = rowsum(dO*O), the main pass, the dQ conversion).  The workload is
+B=4, H=16, N=4096, d=128, bf16, non-causal, with inputs larger than L2
+(Q, K, V, O, dO: 5 x 67 MB).
+
+Printed (rank 0, one JSON line): whole-job TFLOPS (forward 4*B*H*N^2*d plus
+backward 2.5x that, per step time), per-kernel times, the roofline of the
+dominant kernel against the measured peaks, an end-to-end figure through the
+Python API with pinned host buffers, SM clocks sampled during the timed
+region, and the fp64 CPU oracle timed on a bounded sample (cpu_baseline).
+
+``--impl reference`` times the oracle instead (host cores, bounded sample per
+step) and prints the same line shape with "impl": "reference".
+Under torchrun (N > 1) every rank runs its own copy of the workload (weak
+scaling over independent (batch, head) problems; no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import fa_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, d=128) and % of GB300 dense BF16 peak"
+WORKLOAD = fa_inputs.WORKLOADS["fwd_4k"]          # B4 H16 N4096 d128, non-causal
+KERNEL_SOURCES = ["fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "ptx.cuh", "exp2.cuh"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_workload(w: fa_inputs.Workload, rank: int) -> fa_inputs.Workload:
+    """Each rank owns an independent copy of the workload (its own seed)."""
+    return w.with_(seed=w.seed + 1000 * rank)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p["bf16_tflops_sustained"],
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "exact_attention_74_gb300", "csrc", name)
+    if not os.path.exists(path):
+        return ""
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f).get(kernel)
+    if not t:
+        return None
+    for src, h in t.get("source_hashes", {}).items():
+        if kernel_source_hash(src) != h:
+            return None
+    return t.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(w: fa_inputs.Workload, budget_s: float, with_bwd: bool):
+    """Time the fp64 oracle on whole heads of the workload until budget_s passes.
+
+    Returns (flops done, seconds, heads, threads).
+    """
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    one = w.with_(B=1, H=1)
+    flops_head = one.fwd_flops() + (one.bwd_flops() if with_bwd else 0.0)
+    done, heads, secs = 0.0, 0, 0.0
+    while heads == 0 or secs < budget_s:
+        h = one.with_(seed=w.seed + 17 * heads)
+        qb, kb, vb = fa_inputs.make_qkv(h)
+        q, k, v = (fa_inputs.bf16_bits_to_f64(x)[0, 0] for x in (qb, kb, vb))
+        do = fa_inputs.bf16_bits_to_f64(fa_inputs.make_dout(h))[0, 0] if with_bwd else None
+        t1 = time.perf_counter()          # input generation stays outside the timing
+        oracle.head_forward(q, k, v, causal=w.causal, scale=w.scale)
+        if with_bwd:
+            oracle.head_backward(q, k, v, do, causal=w.causal, scale=w.scale)
+        secs += time.perf_counter() - t1
+        done += flops_head
+        heads += 1
+    return done, secs, heads, threads
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOAD
+    steps_t = []
+    for i in range(args.warmup + args.steps):
+        flops, secs, heads, threads = oracle_sample(w, args.ref_budget, with_bwd=True)
+        if i >= args.warmup:
+            steps_t.append((flops, secs, heads))
+    flops = sum(f for f, _, _ in steps_t)
+    secs = sum(s for _, s, _ in steps_t)
+    value = flops / secs / 1e12
+    heads = steps_t[0][2]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / len(steps_t) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"B{w.B} H{w.H} N{w.N_q} d{w.d} non-causal, fwd+bwd",
+                   "sample_per_step": f"{heads} whole heads (B=1,H=1,N={w.N_q},d={w.d})"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{heads} whole heads of the workload per step, fwd+bwd, fp64 numpy"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_gpu(args):
+    import torch
+    import exact_attention_74_gb300 as fa
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = rank_workload(WORKLOAD, rank)
+    B, H, N, d = w.B, w.H, w.N_q, w.d
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v, do = (to_dev(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    causal = int(w.causal)
+
+    def fwd():
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, N, N, d, causal, w.scale, sh)
+        if st != fa.FA_OK:
+            raise fa.FAError(st, "fa_fwd")
+
+    def bwd():
+        return fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                         B, H, N, N, d, causal, w.scale, ws.data_ptr(), ws_bytes, sh)
+
+    fwd()
+    has_bwd = bwd() == fa.FA_OK
+    torch.cuda.synchronize(dev)
+    launches_per_step = 1 + (3 if has_bwd else 0)
+
+    # warm-up
+    for _ in range(args.warmup):
+        fwd()
+        if has_bwd:
+            bwd()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            if has_bwd:
+                bwd()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t_wall
+        if pg:
+            pg.barrier()
+    st = fa.fa_get_last_device_status(sh)
+    if st != fa.FA_OK:
+        raise fa.FAError(st, "device status after timed region")
+    t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    t_bwd = [e[1].elapsed_time(e[2]) for e in ev] if has_bwd else [0.0] * args.steps
+    ms_step = statistics.mean(a + b for a, b in zip(t_fwd, t_bwd))
+    if pg:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    flops_step = w.fwd_flops() + (w.bwd_flops() if has_bwd else 0.0)
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the Python API with pinned host buffers
+    host_in = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in (qb, kb, vb, dob)]
+    host_out = [torch.empty(x.shape, dtype=torch.int16).pin_memory() for x in (qb, qb, kb, vb)]
+    host_lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * 2 for x in host_in)
+    d2h = sum(x.numel() * 2 for x in host_out[: (4 if has_bwd else 1)]) + host_lse.numel() * 4
+
+    def e2e_step():
+        qq, kk, vv, dd = (h.to(dev, non_blocking=True).view(torch.bfloat16) for h in host_in)
+        oo, ll = fa.forward(qq, kk, vv, causal=w.causal, scale=w.scale)
+        outs = [oo]
+        if has_bwd:
+            outs += list(fa.backward(qq, kk, vv, oo, dd, ll, causal=w.causal, scale=w.scale,
+                                     workspace=ws))
+        for hbuf, t in zip(host_out, outs):
+            hbuf.copy_(t.view(torch.int16), non_blocking=True)
+        host_lse.copy_(ll, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if pg:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    # ---- roofline of the dominant kernel
+    peaks = measured_peaks()
+    mean_fwd = statistics.mean(t_fwd)
+    mean_bwd = statistics.mean(t_bwd) if has_bwd else 0.0
+    if mean_bwd > mean_fwd:
+        dom, dom_ms, dom_flops = "fa_bwd", mean_bwd, w.bwd_flops()
+    else:
+        dom, dom_ms, dom_flops = "fa_fwd", mean_fwd, w.fwd_flops()
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peaks['source']} (burst bf16 GEMM)",
+                "traffic": ncu_traffic(dom)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"B{B} H{H} N{N} d{d} non-causal, fwd+bwd" if has_bwd
+                   else f"B{B} H{H} N{N} d{d} non-causal, fwd only (backward not built)",
+                   "l2": "inputs larger than L2 (5 x 67 MB), no flush",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "pct_of_peak": value / world / peaks["bf16_tflops"] * 100.0,
+        "kernels_ms": {"fa_fwd": mean_fwd, "fa_bwd": mean_bwd if has_bwd else None},
+        "fwd_tflops": w.fwd_flops() / (mean_fwd * 1e-3) / 1e12,
+        "bwd_tflops": (w.bwd_flops() / (mean_bwd * 1e-3) / 1e12) if has_bwd else None,
+        "roofline": roofline,
+        "e2e": {"value": flops_step * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": wall,
+        "clocks": clocks.summary(),
+    }
+    if args.sweep:
+        line["sweep"] = sweep(torch, fa, dev, sh)
+    if rank == 0 and not args.no_cpu_baseline:
+        flops, secs, heads, threads = oracle_sample(WORKLOAD, args.cpu_budget, with_bwd=has_bwd)
+        line["cpu_baseline"] = {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{heads} whole heads (B=1,H=1,N={N},d={d}) fwd"
+                                          f"{'+bwd' if has_bwd else ''}, fp64 numpy, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def sweep(torch, fa, dev, sh, reps=10):
+    """Forward TFLOPS over the 16k-token sequence sweep and the 4k / 8k configs."""
+    out = []
+    wls = fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True)
+    wls += [fa_inputs.WORKLOADS["stress_8k"]]
+    for w in wls:
+        qb, kb, vb = fa_inputs.make_qkv(w)
+        q, k, v = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device=dev)
+
+        def call():
+            st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           w.B, w.H, w.N_q, w.N_kv, w.d, int(w.causal), w.scale, sh)
+            assert st == fa.FA_OK
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        out.append({"workload": w.name, "B": w.B, "N": w.N_q, "causal": w.causal, "ms": ms,
+                    "tflops": w.fwd_flops() / (ms * 1e-3) / 1e12})
+        del q, k, v, o, lse
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sweep", action="store_true", help="also time the forward sequence sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=4.0, help="oracle seconds per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps, always
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

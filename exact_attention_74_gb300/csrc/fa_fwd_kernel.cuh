@@ -18,10 +18,14 @@
 // Kernel Pipelining Co-Design for Asymmetric Hardware Scaling"
 // (条件付きオンラインsoftmaxリスケーリング): the row keeps a reference maximum
 // m_ref and P = 2^(t - m_ref); O and l are rescaled by 2^(m_ref - m_new) only
-// when the row maximum rises more than tau above m_ref.  Normalisation by l
-// is deferred to the epilogue (§8.1 of the first page), which also writes
-// LSE = ln2 * (m_ref + log2 l).  Some of the exponentials take the FMA-pipe
-// cubic emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
+// when the row maximum rises more than tau above m_ref.  Normalisation is
+// deferred to the epilogue (§8.1 of the first page), which also writes
+// LSE = ln2 * (m_ref + log2 l).  Two row sums are kept: l over the fp32
+// probabilities (for the LSE) and lr over the bf16-rounded probabilities that
+// the P V product actually consumes; O is divided by lr, so its weights form
+// an exact convex combination even when the largest P of a row (up to 2^tau)
+// is not a power of two.  Some of the exponentials take the FMA-pipe cubic
+// emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
 //
 // Causal masking skips every key tile that lies wholly above the diagonal;
 // only the last key tile of each query tile needs an element mask (it holds
@@ -254,7 +258,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const uint32_t tO = tmem + lane_addr + C::col_O(t);
     const float c = p.c;
     float m_ref = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;      // sum of the fp32 probabilities: gives the LSE
+    float lr = 0.f;     // sum of the bf16-rounded probabilities fed to P V: normalises O
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), j & 1, p.ctl, abort_flag));
@@ -285,6 +290,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         resc = true;
         alpha = ex2_hw(m_ref - m_new);
         l *= alpha;
+        lr *= alpha;
         m_ref = m_new;
       }
       if (__any_sync(0xffffffffu, resc)) {
@@ -298,18 +304,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
       }
       const float neg = -m_ref;
-      float sum[8];
+      float sum[4], sumr[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+      for (int i = 0; i < 4; ++i) sum[i] = sumr[i] = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const float e0 = ex2_mix<EMU>(fmaf(__uint_as_float(s[2 * i]), c, neg), 2 * i);
         const float e1 = ex2_mix<EMU>(fmaf(__uint_as_float(s[2 * i + 1]), c, neg), 2 * i + 1);
-        sum[i & 7] += e0 + e1;
-        pk[i] = pack_bf16x2(e0, e1);
+        const uint32_t w = pack_bf16x2(e0, e1);
+        sum[i & 3] += e0 + e1;
+        sumr[i & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+        pk[i] = w;
       }
-      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      lr += (sumr[0] + sumr[1]) + (sumr[2] + sumr[3]);
       tmem_st_x64(tS, pk);
       tc_fence_before();
       mbar_arrive(bar(C::kPFull + t));
@@ -319,7 +328,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (ready) ready = mbar_wait(bar(C::kOFull + t), 0, p.ctl, abort_flag);
     if (__all_sync(0xffffffffu, ready)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {

@@ -93,9 +93,26 @@ def test_rescale_threshold_on_stress_inputs(torch, tau, emu):
     full_compare(torch, w, tau=tau, emu=emu)
 
 
-def test_outlier_distribution(torch):
-    w = _wl(1, 4, 1024, 1024, 128, False, seed=31, kind="outlier")
-    full_compare(torch, w)
+@pytest.mark.parametrize("causal", [False, True])
+def test_outlier_distribution_accuracy(torch, causal):
+    """N(0,1) + N(0,100)*Bernoulli(0.001) inputs (the FlashAttention-3 notes' error study).
+
+    |O| reaches tens here, where one bf16 step is 0.125, so the absolute 1e-2
+    bound of the iid workloads cannot apply; each element must instead lie
+    within one bf16 step (2^-7 relative) of the exact value, the whole tensor
+    within 5e-3 relative RMS, and the LSE within 1e-3 (+1e-6 relative).
+    """
+    w = _wl(1, 4, 1024, 1024, 128, causal, seed=31, kind="outlier")
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale)
+    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, causal=w.causal, scale=w.scale)
+    err = np.abs(o - o_ref)
+    assert np.all(err <= np.maximum(gu.O_MAX_ABS, 2.0 ** -7 * np.abs(o_ref)))
+    assert gu.rel_rms(o, o_ref) <= gu.O_REL_RMS
+    assert np.all(np.abs(lse - lse_ref) <= gu.LSE_MAX_ABS + 1e-6 * np.abs(lse_ref))
+    rmse = float(np.sqrt(np.mean((o - o_ref) ** 2)))
+    print(f"outlier inputs causal={causal}: O RMSE vs fp64 {rmse:.3e}")
 
 
 def sampled_compare(torch, w, heads, nrows, **kw):
