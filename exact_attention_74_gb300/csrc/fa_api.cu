@@ -164,9 +164,10 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
   if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N_q;
+  const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(N_q) + 127) / 128 * 128);
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
-  const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
-  return acc + delta;
+  const size_t vec = (rows_pad * sizeof(float) + 255) / 256 * 256;
+  return acc + 2 * vec;
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
@@ -208,7 +209,6 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   a.scale = scale;
   a.stream = static_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_bwd(a);
-  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -228,7 +228,9 @@ int fa_get_last_device_status(fa_stream_t stream) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }
-  return (v & kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+  if (v & kStatusTimeout) return FA_ERR_TIMEOUT;
+  if (v & kStatusLaunchConfig) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
 }
 
 int fa_set_wait_timeout_ns(unsigned long long ns) {

@@ -1,0 +1,458 @@
+// fa_bwd_kernel.cuh -- backward exact attention for sm_103a.
+//
+// The backward pass recomputes S and P from the saved LSE instead of storing
+// them ("FlashAttention: GPUメモリ階層を活用したアテンション最適化の分析" §7.2)
+// and keeps its intermediates in tensor memory ("論文解説: FlashAttention-4 —
+// Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware Scaling",
+// Backwardパスの最適化).  With D_i = sum_c dO_ic O_ic it forms
+//   P = exp(scale q.k - LSE),  dP = dO V^T,  dS = P o (dP - D),
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three kernels:
+//   prep  -- per query row: D, LSE * log2(e) (both padded to a multiple of 128
+//            rows per head: padding rows get D = 0, LSE = +inf so their P is 0),
+//            and clears the fp32 dQ accumulator.
+//   main  -- one CTA per (128-key tile, batch*head), K and V resident in shared
+//            memory, looping over the query tiles that can see its keys
+//            (causal: only tiles at or below the diagonal):
+//              warp 0    TMA producer (Q, dO tiles, LSE and D rows, 2 stages)
+//              warp 1    MMA issuer: S^T = K Q^T, dP^T = V dO^T into tensor
+//                        memory; then dV += P^T dO (P read from tensor
+//                        memory), dK += dS^T Q and the partial dQ = dS K (dS
+//                        read from shared memory in its two orientations)
+//              warps 2-5 one key row per thread: P, dS; P back into tensor
+//                        memory, dS into shared memory (128-byte swizzle)
+//              warps 6-9 drain each partial dQ from tensor memory into the
+//                        fp32 accumulator with vector atomic adds
+//            dK and dV stay in tensor memory for the whole loop and are
+//            written once at the end.
+//   convert -- dQ = bf16(scale * accumulator).
+// Tensor-memory columns: S^T/P^T [0,128), dP^T and then the partial dQ
+// [128,256), dV [256,256+D), dK [256+D,256+2D).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+#include "exp2.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kBM = 128;          // keys per CTA
+constexpr int kBN = 128;          // queries per step
+constexpr int kThreads = 320;
+constexpr int kPanel = 128 * 128; // 128 rows x 128 B swizzle panel
+
+template <int D>
+struct Cfg {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kTile;
+  static constexpr int kStage0 = 2 * kTile;
+  static constexpr int kStageBytes = 2 * kTile + 1024;    // Q, dO, lse2[128], delta[128]
+  static constexpr int kDS = kStage0 + 2 * kStageBytes;   // dS^T tile, 2 panels of 128 keys x 64 queries
+  static constexpr int kBar = kDS + 2 * kPanel;
+  // barrier indices
+  static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
+                       kDQFree = 8, kAccFull = 9, kNumBars = 10;
+  static constexpr int kMisc = kBar + 8 * kNumBars;
+  static constexpr int kSmem = kMisc + 16;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static __device__ constexpr int q_off(int s) { return kStage0 + s * kStageBytes; }
+  static __device__ constexpr int do_off(int s) { return kStage0 + s * kStageBytes + kTile; }
+  static __device__ constexpr int lse_off(int s) { return kStage0 + s * kStageBytes + 2 * kTile; }
+  static __device__ constexpr int dlt_off(int s) { return kStage0 + s * kStageBytes + 2 * kTile + 512; }
+};
+
+struct Params {
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse2;     // [BH, nq_pad]
+  const float* delta;    // [BH, nq_pad]
+  int BH, N_q, N_kv, nq_pad, causal;
+  int n_q_tiles, n_kv_tiles;
+  float c;               // scale * log2(e)
+  float scale;
+  DevCtl ctl;
+};
+
+// ------------------------------------------------------------------- prep
+
+template <int D>
+__global__ void __launch_bounds__(256)
+prep_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+            const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
+            float* __restrict__ dq_acc, int BH, int N_q, int nq_pad) {
+  constexpr int kPer = D / 32;     // elements per lane
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(BH) * nq_pad;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows;
+       r += warps) {
+    const int bh = static_cast<int>(r / nq_pad);
+    const int q = static_cast<int>(r % nq_pad);
+    if (q < N_q) {
+      const size_t base = (static_cast<size_t>(bh) * N_q + q) * D + lane * kPer;
+      float acc = 0.f;
+      if constexpr (kPer == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(O + base);
+        const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
+        const uint32_t aw[2] = {a.x, a.y}, bw[2] = {b.x, b.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
+          acc = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(bw[i] & 0xffff0000u), acc);
+        }
+        *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        const uint32_t a = *reinterpret_cast<const uint32_t*>(O + base);
+        const uint32_t b = *reinterpret_cast<const uint32_t*>(dO + base);
+        acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
+        acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
+        *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) {
+        delta[r] = acc;
+        lse2[r] = lse[static_cast<size_t>(bh) * N_q + q] * 1.4426950408889634f;
+      }
+    } else if (lane == 0) {
+      delta[r] = 0.f;
+      lse2[r] = INFINITY;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- convert
+
+__global__ void __launch_bounds__(256)
+convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8, float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 w;
+    w.x = pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = pack_bf16x2(a.z * scale, a.w * scale);
+    w.z = pack_bf16x2(b.x * scale, b.y * scale);
+    w.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = w;
+  }
+}
+
+// ------------------------------------------------------------------- main
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+            const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {   // operand atoms need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(p.ctl.status, kStatusLaunchConfig);
+    return;
+  }
+  auto bar = [&](int i) -> uint32_t { return sb + C::kBar + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int j, bh;
+  if (p.causal) {   // key tile 0 sees every query tile: run the heaviest first
+    j = static_cast<int>(blockIdx.x) / p.BH;
+    bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else {
+    j = static_cast<int>(blockIdx.x) % p.n_kv_tiles;
+    bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
+  }
+  const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
+  const int n_it = max(0, p.n_q_tiles - i0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kKVFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kQFull + s), 1);
+      mbar_init(bar(C::kQEmpty + s), 1 + 4);   // MMA commit + one arrive per compute warp
+    }
+    mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kPFull), 128);
+    mbar_init(bar(C::kDQFull), 1);
+    mbar_init(bar(C::kDQFree), 128);
+    mbar_init(bar(C::kAccFull), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (n_it > 0 && warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmdO);
+      mbar_arrive_expect_tx(bar(C::kKVFull), 2 * C::kTile);
+      for (int pn = 0; pn < D / 64; ++pn) {
+        tma_load_3d(sb + C::kK + pn * kPanel, &tmK, bar(C::kKVFull), pn * 64, j * kBM, bh);
+        tma_load_3d(sb + C::kV + pn * kPanel, &tmV, bar(C::kKVFull), pn * 64, j * kBM, bh);
+      }
+      const uint64_t keep = l2_policy_evict_last();
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(bar(C::kQEmpty + s), ((it >> 1) & 1) ^ 1, p.ctl, abort_flag)) break;
+        const int i = i0 + it;
+        const uint32_t fb = bar(C::kQFull + s);
+        mbar_arrive_expect_tx(fb, 2 * C::kTile + 1024);
+        for (int pn = 0; pn < D / 64; ++pn) {
+          tma_load_3d_hint(sb + C::q_off(s) + pn * kPanel, &tmQ, fb, pn * 64, i * kBN, bh, keep);
+          tma_load_3d_hint(sb + C::do_off(s) + pn * kPanel, &tmdO, fb, pn * 64, i * kBN, bh, keep);
+        }
+        const size_t row = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * kBN;
+        bulk_load(sb + C::lse_off(s), p.lse2 + row, 512, fb);
+        bulk_load(sb + C::dlt_off(s), p.delta + row, 512, fb);
+      }
+    }
+  } else if (n_it > 0 && warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t idKV = idesc_bf16(kBM, D, false, true);
+      constexpr uint32_t idQ = idesc_bf16(kBN, D, true, true);
+      const uint32_t sK = sb + C::kK, sV = sb + C::kV, sDS = sb + C::kDS;
+      bool ok = mbar_wait(bar(C::kKVFull), 0, p.ctl, abort_flag);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it & 1;
+        ok = mbar_wait(bar(C::kQFull + s), (it >> 1) & 1, p.ctl, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sQ = sb + C::q_off(s), sdO = sb + C::do_off(s);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {     // S^T = K Q^T
+          const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
+          mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 0, 1024), sdesc_sw128(sQ + off, 0, 1024), idS, k > 0);
+        }
+        if (it > 0) {   // the partial dQ of the previous tile must be drained first
+          ok = mbar_wait(bar(C::kDQFree), (it - 1) & 1, p.ctl, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {     // dP^T = V dO^T
+          const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
+          mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 0, 1024), sdesc_sw128(sdO + off, 0, 1024), idS, k > 0);
+        }
+        tc_commit(bar(C::kSFull));
+        ok = mbar_wait(bar(C::kPFull), it & 1, p.ctl, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {   // dV += P^T dO
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k, sdesc_sw128(sdO + k * 2048, kPanel, 1024), idKV,
+                 (it > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {   // dK += dS^T Q  (unscaled)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
+                 sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k) {   // dQ_i = dS K  (unscaled partial)
+          mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + k * 2048, kPanel, 1024),
+                 sdesc_sw128(sK + k * 2048, kPanel, 1024), idQ, k > 0);
+        }
+        tc_commit(bar(C::kDQFull));
+        tc_commit(bar(C::kQEmpty + s));
+      }
+      if (ok) tc_commit(bar(C::kAccFull));
+    }
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------- P and dS rows
+    const int rank = warp & 3;
+    const int r = rank * 32 + lane;          // key row within the tile
+    const int kg = j * kBM + r;              // global key index
+    const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
+    const bool key_ok = kg < p.N_kv;
+    const float2 c2 = make_float2(p.c, p.c);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      const int i = i0 + it;
+      bool w = mbar_wait(bar(C::kSFull), it & 1, p.ctl, abort_flag);
+      if (w) w = mbar_wait(bar(C::kQFull + s), (it >> 1) & 1, p.ctl, abort_flag);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse_s = reinterpret_cast<const float*>(smem + C::lse_off(s));
+      const float* dlt_s = reinterpret_cast<const float*>(smem + C::dlt_off(s));
+      // queries q with q_g < k_g are masked (causal); only the diagonal tile has any
+      const int lim = (p.causal && i == j) ? r : 0;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], dp[32];
+        tmem_ld_x32(tmem + lane_addr + C::kColS + 32 * ch, sv);
+        tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * ch + u);
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + 32 * ch + u);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q = u + 2 * h;          // column within the chunk
+            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+            const float2 x = fma2(make_float2(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1])), c2, nl);
+            float p0 = ex2_hw(x.x), p1 = ex2_hw(x.y);
+            const int qc = 32 * ch + q;
+            if (!key_ok || qc < lim) p0 = 0.f;
+            if (!key_ok || qc + 1 < lim) p1 = 0.f;
+            const float2 t = add2(make_float2(__uint_as_float(dp[q]), __uint_as_float(dp[q + 1])), nd);
+            const float2 ds = mul2(make_float2(p0, p1), t);
+            pk[q >> 1] = pack_bf16x2(p0, p1);
+            dk[q >> 1] = pack_bf16x2(ds.x, ds.y);
+          }
+        }
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * ch, pk);
+        // dS^T row r, queries 32ch..32ch+31: panel ch/2, 16-byte chunks (ch&1)*4 + u
+        uint8_t* rowp = smem + C::kDS + (ch >> 1) * kPanel + r * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = ((ch & 1) * 4 + u) ^ (r & 7);
+          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::kPFull));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kQEmpty + s));
+    }
+    // ----------------------------------------------------- dK, dV epilogue
+    bool ready = ok;
+    if (n_it > 0 && ready) ready = mbar_wait(bar(C::kAccFull), 0, p.ctl, abort_flag);
+    ready = __all_sync(0xffffffffu, ready);
+    if (n_it == 0 || ready) {
+      if (n_it > 0) tc_fence_after();
+      const size_t rowoff = (static_cast<size_t>(bh) * p.N_kv + kg) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* outp = (which == 0 ? p.dv : p.dk) + rowoff;
+        const float f = which == 0 ? 1.f : p.scale;
+        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          if (n_it > 0) {
+            tmem_ld_x32(tmem + lane_addr + col + 32 * ch, v);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) v[u] = 0u;
+          }
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(outp + 32 * ch);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16x2(__uint_as_float(v[8 * u + 2 * e]) * f, __uint_as_float(v[8 * u + 2 * e + 1]) * f);
+              dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      }
+    }
+  } else if (n_it > 0 && warp >= 6) {
+    // -------------------------------------------------------- dQ drainage
+    const int rank = warp & 3;
+    const int r = rank * 32 + lane;          // query row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
+    for (int it = 0; it < n_it; ++it) {
+      const int qg = (i0 + it) * kBN + r;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), it & 1, p.ctl, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.N_q + qg) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, v);
+        if (qg < p.N_q) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + 32 * ch + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                       __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kDQFree));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch(const BwdLaunch& a) {
+  using C = Cfg<D>;
+  const int nq_pad = (a.N_q + kBN - 1) / kBN * kBN;
+  // workspace: dq_acc [BH*N_q*D] (rounded to 256 B), then delta, lse2 [BH*nq_pad] each
+  float* lse2 = a.delta + static_cast<size_t>(a.BH) * nq_pad;
+  {
+    const long long rows = static_cast<long long>(a.BH) * nq_pad;
+    const long long blocks = (rows + 7) / 8;
+    prep_kernel<D><<<static_cast<unsigned>(blocks < 65535 * 8 ? blocks : 65535 * 8), 256, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, lse2, a.delta,
+        a.dq_acc, a.BH, a.N_q, nq_pad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  Params p;
+  p.dq_acc = a.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.lse2 = lse2;
+  p.delta = a.delta;
+  p.BH = a.BH;
+  p.N_q = a.N_q;
+  p.N_kv = a.N_kv;
+  p.nq_pad = nq_pad;
+  p.causal = a.causal;
+  p.n_q_tiles = nq_pad / kBN;
+  p.n_kv_tiles = (a.N_kv + kBM - 1) / kBM;
+  p.c = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.scale = a.scale;
+  p.ctl = a.ctl;
+  auto kern = main_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.n_kv_tiles) * p.BH;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmem, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n8 = static_cast<long long>(a.BH) * a.N_q * D / 8;
+  const long long blocks = (n8 + 255) / 256;
+  convert_kernel<<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, a.stream>>>(
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8, a.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+}  // namespace fa

@@ -274,13 +274,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = __float_as_uint(-INFINITY);
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
+      for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(s[i]);
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(s[i]));
-      const float m_blk = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 4; i < 128; i += 8) {
+        mx[0] = max3(mx[0], __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+        mx[1] = max3(mx[1], __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+        mx[2] = max3(mx[2], __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
+        mx[3] = max3(mx[3], __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+      }
+      const float m_blk = c * fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
       const float m_new = fmaxf(m_ref, m_blk);
       bool resc = false;
       float alpha = 1.f;
@@ -299,25 +303,32 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           uint32_t o[32];
           tmem_ld_x32(tO + 32 * ch, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                  make_float2(alpha, alpha));
+            o[i] = __float_as_uint(r.x);
+            o[i + 1] = __float_as_uint(r.y);
+          }
           tmem_st_x32(tO + 32 * ch, o);
         }
       }
-      const float neg = -m_ref;
-      float sum[4], sumr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sum[i] = sumr[i] = 0.f;
+      const float2 c2 = make_float2(c, c);
+      const float2 neg2 = make_float2(-m_ref, -m_ref);
+      float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float sumr[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float e0 = ex2_mix<EMU>(fmaf(__uint_as_float(s[2 * i]), c, neg), 2 * i);
-        const float e1 = ex2_mix<EMU>(fmaf(__uint_as_float(s[2 * i + 1]), c, neg), 2 * i + 1);
+        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+        const float e0 = ex2_mix<EMU>(x.x, 2 * i);
+        const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
+        sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
         const uint32_t w = pack_bf16x2(e0, e1);
-        sum[i & 3] += e0 + e1;
-        sumr[i & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+        sumr[(i & 1) * 2] = add_bf16_lo(w, sumr[(i & 1) * 2]);
+        sumr[(i & 1) * 2 + 1] = add_bf16_hi(w, sumr[(i & 1) * 2 + 1]);
         pk[i] = w;
       }
-      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      l += (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
       lr += (sumr[0] + sumr[1]) + (sumr[2] + sumr[3]);
       tmem_st_x64(tS, pk);
       tc_fence_before();

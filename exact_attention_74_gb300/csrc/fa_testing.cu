@@ -33,7 +33,7 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const uint32_t bar_full = sb + 2 * tile_bytes, bar_done = bar_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 2 * tile_bytes + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 2 * tile_bytes + 20);
-  const bool b_mn = mode & 1, a_tmem = mode & 2;
+  const bool b_mn = mode & 1, a_tmem = mode & 2, a_mn = mode & 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -50,8 +50,13 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(bar_full, (a_tmem ? 0 : tile_bytes) + tile_bytes);
-    for (int pn = 0; pn < K / 64 && !a_tmem; ++pn)
-      tma_load_3d(sA + pn * 16384, &tmA, bar_full, pn * 64, 0, 0);
+    if (a_mn) {
+      // A is [K, 128]: two 64-column panels of K rows each
+      for (int pn = 0; pn < 2; ++pn) tma_load_3d(sA + pn * K * 128, &tmA, bar_full, pn * 64, 0, 0);
+    } else {
+      for (int pn = 0; pn < K / 64 && !a_tmem; ++pn)
+        tma_load_3d(sA + pn * 16384, &tmA, bar_full, pn * 64, 0, 0);
+    }
     if (!b_mn) {
       for (int pn = 0; pn < K / 64; ++pn) tma_load_3d(sB + pn * 16384, &tmB, bar_full, pn * 64, 0, 0);
     } else {
@@ -76,12 +81,14 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     if (mbar_wait(bar_full, 0, ctl, abort_flag)) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 128, false, b_mn);
+      const uint32_t idesc = idesc_bf16(128, 128, a_mn, b_mn);
       for (int k = 0; k < K / 16; ++k) {
         const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, K * 128, 1024)
                                  : sdesc_sw128(sB + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024);
         if (a_tmem)
           mma_ts(tmem, tmem + 128 + 8 * k, bd, idesc, k > 0);
+        else if (a_mn)
+          mma_ss(tmem, sdesc_sw128(sA + k * 2048, K * 128, 1024), bd, idesc, k > 0);
         else
           mma_ss(tmem, sdesc_sw128(sA + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024), bd, idesc, k > 0);
       }
@@ -141,14 +148,18 @@ int fa_test_exp2(const float* x, float* y, long long n, int mode, fa_stream_t st
 }
 
 int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode, fa_stream_t stream) {
-  if (!A || !B || !C || (K != 64 && K != 128) || mode < 0 || mode > 3) return FA_ERR_INVALID;
+  if (!A || !B || !C || (K != 64 && K != 128) || mode < 0 || mode > 5) return FA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) % 16)
     return FA_ERR_ALIGN;
   DevCtl ctl;
   int st = device_ctl(&ctl);
   if (st != FA_OK) return st;
   CUtensorMap tmA, tmB;
-  if ((st = make_map_bf16(&tmA, A, K, 128, 1)) != FA_OK) return st;
+  if (mode & 4)
+    st = make_map_bf16(&tmA, A, 128, K, 1, K);   // [K, 128]: panels of 64 columns, K rows
+  else
+    st = make_map_bf16(&tmA, A, K, 128, 1);
+  if (st != FA_OK) return st;
   if (mode & 1)
     st = make_map_bf16(&tmB, B, 128, K, 1, K);   // [K, 128]: panels of 64 columns, K rows
   else

@@ -88,8 +88,10 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 /*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for this
- * problem: an fp32 dQ accumulator [B, H, N_q, d] and D = rowsum(dO * O)
- * [B, H, N_q] fp32, each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ * problem: an fp32 dQ accumulator [B, H, N_q, d], then two fp32 row vectors
+ * D = rowsum(dO * O) and LSE * log2(e), each [B, H, N_q rounded up to a
+ * multiple of 128]; every part is rounded up to 256 bytes.  Returns 0 for
+ * invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
 
@@ -111,7 +113,9 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
  * fa_get_last_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns FA_OK, FA_ERR_TIMEOUT if
  * a bounded wait in any kernel of this library ran out since the last call,
- * or FA_ERR_CUDA if the synchronisation itself failed.
+ * FA_ERR_UNSUPPORTED if a kernel found its launch unusable on this device
+ * (it then returned without computing), or FA_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 int fa_get_last_device_status(fa_stream_t stream);
 

@@ -27,8 +27,8 @@ extern "C" {
  *   mode 0: the hardware ex2 unit (approximate, flush-to-zero).
  *   mode 1: the cubic emulation: n = floor(x), f = x - n,
  *           p(f) = 1 + 0.6951 f + 0.2276 f^2 + 0.0771 f^3, exponent n added
- *           to p's exponent field by an integer operation; inputs below -127
- *           are clamped to -127.
+ *           to p's exponent field by an integer operation; inputs below -126
+ *           are clamped to -126 (so the result never drops below 2^-126).
  *   n >= 0 (0 launches nothing); x, y 4-byte aligned.
  */
 int fa_test_exp2(const float* x, float* y, long long n, int mode, fa_stream_t stream);
@@ -42,6 +42,10 @@ int fa_test_exp2(const float* x, float* y, long long n, int mode, fa_stream_t st
  *                     B operand N-major (the O += P V form);
  *   mode bit 1 set:   A is first copied into tensor memory and the product
  *                     reads it from there (the P operand's path);
+ *   mode bit 2 set:   A is given as [K, 128] row-major, i.e. C = A^T * ...
+ *                     with the A operand M-major (the dQ = dS K form);
+ *                     not combined with bit 1.
+ *   Valid modes: 0, 1, 2, 3, 4, 5.
  *   C fp32 [128, 128] row-major (output).
  */
 int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode,

@@ -14,7 +14,6 @@ O_MAX_ABS = 1e-2
 O_REL_RMS = 5e-3
 LSE_MAX_ABS = 1e-3
 GRAD_REL_RMS = 1e-2
-GUARD = 64            # elements of guard band on each side (128 B, keeps 16 B alignment)
 
 
 def torch():
@@ -28,20 +27,26 @@ def dev_bf16(bits):
 
 
 class Guarded:
-    """A device buffer with NaN-filled guard bands around the usable view."""
+    """A device buffer with all-ones (NaN for floats) guard bands of 256 bytes
+    on each side of the usable view, which keeps the view 256-byte aligned."""
 
     def __init__(self, shape, dtype):
         t = torch()
         n = int(np.prod(shape))
-        self.raw = t.empty(n + 2 * GUARD, dtype=dtype, device="cuda")
-        self.raw.view(t.int16 if dtype == t.bfloat16 else t.int32).fill_(-1)   # NaN bit patterns
-        self.view = self.raw[GUARD:GUARD + n].view(shape)
+        self.g = 256 // t.empty((), dtype=dtype).element_size()
+        self.raw = t.empty(n + 2 * self.g, dtype=dtype, device="cuda")
+        self._bits().fill_(-1 if self.raw.dtype != t.uint8 else 255)
+        self.view = self.raw[self.g:self.g + n].view(shape)
+
+    def _bits(self):
+        t = torch()
+        return self.raw.view({t.bfloat16: t.int16, t.float32: t.int32}.get(self.raw.dtype, self.raw.dtype))
 
     def guards_intact(self):
         t = torch()
-        w = t.int16 if self.raw.dtype == t.bfloat16 else t.int32
-        g = t.cat([self.raw[:GUARD], self.raw[-GUARD:]]).view(w)
-        return bool((g == -1).all().item())
+        b = self._bits()
+        g = t.cat([b[:self.g], b[-self.g:]])
+        return bool((g == (255 if self.raw.dtype == t.uint8 else -1)).all().item())
 
 
 def to_f64(t):

@@ -101,9 +101,10 @@ def test_lse_needs_only_4_byte_alignment(lib):
 
 
 def test_workspace_bytes(lib):
-    # fp32 dQ accumulator + fp32 D, each rounded up to 256 bytes
-    assert fa.fa_bwd_workspace_bytes(2, 16, 8192, 8192, 128) == 2 * 16 * 8192 * 128 * 4 + 2 * 16 * 8192 * 4
-    assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 64) == 768 + 256
+    # fp32 dQ accumulator + two fp32 row vectors padded to 128 rows, each rounded to 256 B
+    assert fa.fa_bwd_workspace_bytes(2, 16, 8192, 8192, 128) == 2 * 16 * 8192 * (128 * 4 + 2 * 4)
+    assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 64) == 768 + 2 * 512
+    assert fa.fa_bwd_workspace_bytes(3, 1, 130, 5, 128) == 3 * 130 * 128 * 4 + 2 * 3 * 256 * 4
     assert fa.fa_bwd_workspace_bytes(1, 1, 0, 5, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 80) == 0
 
@@ -146,7 +147,8 @@ def test_testing_entry_point_argument_errors(lib):
     assert fa.fa_test_exp2(P, P, 10, 2, 0) == fa.FA_ERR_INVALID
     assert fa.fa_test_exp2(None, None, 0, 0, 0) == fa.FA_OK     # empty: launches nothing
     assert fa.fa_test_mma_tile(P, P, P, 96, 0, 0) == fa.FA_ERR_INVALID
-    assert fa.fa_test_mma_tile(P, P, P, 64, 4, 0) == fa.FA_ERR_INVALID
+    assert fa.fa_test_mma_tile(P, P, P, 64, 6, 0) == fa.FA_ERR_INVALID
+    assert fa.fa_test_mma_tile(P, P, P, 64, -1, 0) == fa.FA_ERR_INVALID
     assert fa.fa_test_mma_tile(P + 8, P, P, 64, 0, 0) == fa.FA_ERR_ALIGN
     assert fa.fa_test_wait_timeout(5, 0) == fa.FA_ERR_INVALID
 

@@ -1,0 +1,115 @@
+"""Backward parity: fa_bwd (through the C ABI) against the fp64 oracle's exact gradients.
+
+The GPU backward consumes the GPU forward's own bf16 O and fp32 LSE; the
+oracle differentiates <dO, O> at the same bf16 inputs in float64.  dQ, dK and
+dV must each lie within 1e-2 relative RMS.  Small and ragged problems are
+compared over every element; the full-size backward workload (B=2, H=16,
+N=8192, d=128, causal) runs at full size and is compared on whole sampled
+heads.  Outputs start as NaN inside guard bands, and the workspace starts
+as garbage, so unwritten elements, stray writes and a missing clear all show.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import exact_attention_74_gb300 as fa
+import fa_inputs
+import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    assert torch.cuda.is_available()
+    fa.library()
+    return torch
+
+
+def run_fwd_bwd(torch, w, qb, kb, vb, dob):
+    B, H, N_q, d = qb.shape
+    N_kv = kb.shape[2]
+    q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N_q), dtype=torch.float32, device="cuda")
+    st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                   B, H, N_q, N_kv, d, int(w.causal), w.scale, 0)
+    assert st == fa.FA_OK
+    dq = gu.Guarded((B, H, N_q, d), torch.bfloat16)
+    dk = gu.Guarded((B, H, N_kv, d), torch.bfloat16)
+    dv = gu.Guarded((B, H, N_kv, d), torch.bfloat16)
+    need = fa.fa_bwd_workspace_bytes(B, H, N_q, N_kv, d)
+    ws = gu.Guarded((need,), torch.uint8)
+    ws.view.fill_(0xFF)                                   # garbage (NaN patterns) on entry
+    st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                   lse.data_ptr(), dq.view.data_ptr(), dk.view.data_ptr(), dv.view.data_ptr(),
+                   B, H, N_q, N_kv, d, int(w.causal), w.scale, ws.view.data_ptr(), need, 0)
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    for g in (dq, dk, dv):
+        assert g.guards_intact()
+    return gu.to_f64(dq.view), gu.to_f64(dk.view), gu.to_f64(dv.view)
+
+
+def check_grads(got, ref, what):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.all(np.isfinite(g)), f"{what}: non-finite {name}"
+        e = gu.rel_rms(g, r)
+        assert e <= gu.GRAD_REL_RMS, f"{what}: {name} rel-RMS {e:.3e}"
+
+
+def full_compare(torch, w):
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    got = run_fwd_bwd(torch, w, qb, kb, vb, dob)
+    q, k, v, do = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb, dob))
+    ref = oracle.attention_backward(q, k, v, do, causal=w.causal, scale=w.scale)
+    check_grads(got, ref, w.name)
+
+
+def _wl(B, H, N_q, N_kv, d, causal, seed=11, kind="iid"):
+    return fa_inputs.Workload(f"bwd B{B}H{H}q{N_q}kv{N_kv}d{d}c{int(causal)}", B, H, N_q, N_kv, d,
+                              causal, 1.0 / math.sqrt(d), seed, kind)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_d64(torch, causal):
+    full_compare(torch, fa_inputs.WORKLOADS["tiny_causal" if causal else "tiny"])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 17, 128, 129, 300, 640])
+def test_ragged_square(torch, d, causal, n):
+    full_compare(torch, _wl(1, 2, n, n, d, causal, seed=n + d))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nkv", [(100, 300), (300, 100), (1, 513), (513, 1), (256, 384)])
+def test_ragged_rectangular(torch, d, causal, nq, nkv):
+    full_compare(torch, _wl(2, 1, nq, nkv, d, causal, seed=nq * 3 + nkv))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_medium_multi_head(torch, causal):
+    full_compare(torch, _wl(2, 3, 1024, 1024, 128, causal, seed=5))
+
+
+def test_stress_inputs(torch):
+    w = fa_inputs.WORKLOADS["stress_8k"].with_(B=1, H=2, N_q=1024, N_kv=1024)
+    full_compare(torch, w)
+
+
+def test_full_size_backward(torch):
+    w = fa_inputs.WORKLOADS["bwd_8k"]
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    dq, dk, dv = run_fwd_bwd(torch, w, qb, kb, vb, dob)
+    for b, h in ((0, 0), (1, 13)):
+        q, k, v, do = (fa_inputs.bf16_bits_to_f64(x[b, h]) for x in (qb, kb, vb, dob))
+        ref = oracle.head_backward(q, k, v, do, causal=w.causal, scale=w.scale)
+        check_grads((dq[b, h], dk[b, h], dv[b, h]), ref, f"{w.name} b{b} h{h}")

@@ -63,18 +63,18 @@ def test_exp2_masked_input_is_negligible(torch):
 
 
 @pytest.mark.parametrize("K", [64, 128])
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5])
 def test_mma_tile(torch, K, mode):
     rng = np.random.default_rng(1000 + K + mode)
-    a_bits = fa_inputs_bits(rng, (128, K))
-    b_shape = (K, 128) if mode & 1 else (128, K)
-    b_bits = fa_inputs_bits(rng, b_shape)
+    a_bits = fa_inputs_bits(rng, (K, 128) if mode & 4 else (128, K))
+    b_bits = fa_inputs_bits(rng, (K, 128) if mode & 1 else (128, K))
     A, B = gu.dev_bf16(a_bits), gu.dev_bf16(b_bits)
     C = torch.full((128, 128), float("nan"), dtype=torch.float32, device="cuda")
     assert fa.fa_test_mma_tile(A.data_ptr(), B.data_ptr(), C.data_ptr(), K, mode, 0) == fa.FA_OK
     assert fa.fa_get_last_device_status(0) == fa.FA_OK
     a = gu.fa_inputs.bf16_bits_to_f64(a_bits)
     b = gu.fa_inputs.bf16_bits_to_f64(b_bits)
+    a = a.T if mode & 4 else a
     ref = a @ b if mode & 1 else a @ b.T
     got = C.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-5
