@@ -403,20 +403,50 @@ def sweep(torch, fa, dev, sh, reps=10):
     return out
 
 
+def run_profile_case(args):
+    """fwd + bwd on one named workload, W + K times, for ncu captures (prints ms only)."""
+    import torch
+    import exact_attention_74_gb300 as fa
+    w = fa_inputs.WORKLOADS[args.profile]
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in (qb, kb, vb, dob))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d), dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            e0.record()
+        o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
+        if not args.fwd_only:
+            fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    st = fa.fa_get_last_device_status(torch.cuda.current_stream().cuda_stream)
+    if st != fa.FA_OK:
+        raise fa.FAError(st, "device status")
+    print(json.dumps({"profile_case": w.name, "ms_per_step": e0.elapsed_time(e1) / max(1, args.steps)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sweep", action="store_true", help="also time the forward sequence sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-budget", type=float, default=4.0, help="oracle seconds per reference step")
+    ap.add_argument("--profile", choices=sorted(fa_inputs.WORKLOADS), default=None,
+                    help="only run fwd+bwd on this workload (for profiler captures)")
+    ap.add_argument("--fwd-only", action="store_true", help="with --profile: forward only")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps, always
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile_case(args)
     return run_gpu(args)
 
 

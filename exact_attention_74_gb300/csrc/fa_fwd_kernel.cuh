@@ -274,11 +274,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = __float_as_uint(-INFINITY);
       }
-      float mx[4];
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(s[i]);
-#pragma unroll
-      for (int i = 4; i < 128; i += 8) {
+      for (int i = 0; i < 128; i += 8) {
         mx[0] = max3(mx[0], __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
         mx[1] = max3(mx[1], __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
         mx[2] = max3(mx[2], __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));

@@ -7,5 +7,6 @@ the passages each one follows.
 """
 from .attention import (  # noqa: F401
     EXP2_POLY, attention_backward, attention_forward, exp2_cubic,
-    head_backward, head_forward, online_softmax_forward, softmax_probs,
+    head_backward, head_backward_from_saved, head_forward, online_softmax_forward,
+    softmax_probs,
 )

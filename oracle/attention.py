@@ -25,7 +25,10 @@ are silent or garbled:
   (the square ``tril`` mask of [FA] §11.3, extended to N_q != N_kv).
 * LSE is the natural-log log-sum-exp of the scaled scores, fp32 on the GPU.
 * The backward pass is the exact gradient of <dO, O> at the given inputs
-  ([FA] §7.2 only says S and P are recomputed from the saved statistics).
+  ([FA] §7.2 only says S and P are recomputed from the saved statistics);
+  ``head_backward_from_saved`` is the same computation driven by a given
+  (saved, possibly rounded) O and LSE, which is what a backward kernel
+  receives.
 * Conditional rescaling keeps a reference maximum m_ref per row; P is
   2^(t - m_ref) while the row max has not risen more than tau above m_ref
   (so P may reach 2^tau); when it has, O and l are multiplied by
@@ -40,6 +43,7 @@ import numpy as np
 
 __all__ = [
     "head_forward", "attention_forward", "attention_backward", "head_backward",
+    "head_backward_from_saved",
     "online_softmax_forward", "exp2_cubic", "EXP2_POLY", "softmax_probs",
 ]
 
@@ -144,6 +148,38 @@ def attention_backward(q, k, v, do, *, causal: bool, scale: float):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h] = head_backward(
                 q[b, h], k[b, h], v[b, h], do[b, h], causal=causal, scale=scale)
+    return dq, dk, dv
+
+
+def head_backward_from_saved(q, k, v, o, do, lse, *, causal: bool, scale: float):
+    """Gradients for one head from saved forward outputs (float64).
+
+    The recomputation contract of [FA] §7.2 taken literally: the forward
+    saved O and the row statistics (here the natural-log LSE), and the
+    backward rebuilds P = exp(scale q k^T - LSE) from them instead of
+    renormalising.  With D_i = sum_c dO_ic o_ic for the GIVEN o:
+    dV = P^T dO, dS = P o (dO V^T - D), dQ = scale dS K, dK = scale dS^T Q.
+    Fed this oracle's own O and LSE it equals ``head_backward``; fed a rounded
+    O (as a bf16 forward output would be) it gives what a backward pass
+    computes from that O.
+    """
+    n, n_kv = q.shape[0], k.shape[0]
+    D = np.sum(do * o, axis=1)
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rb = _row_block(n_kv)
+    for r0 in range(0, n, rb):
+        sl = slice(r0, min(n, r0 + rb))
+        s = scale * (q[sl] @ k.T)
+        if causal:
+            rows = np.arange(sl.start, sl.stop)
+            s = np.where(np.arange(n_kv)[None, :] <= rows[:, None], s, -np.inf)
+        p = np.exp(s - lse[sl, None])
+        dv += p.T @ do[sl]
+        ds = p * (do[sl] @ v.T - D[sl, None])
+        dq[sl] = scale * (ds @ k)
+        dk += scale * (ds.T @ q[sl])
     return dq, dk, dv
 
 

@@ -244,6 +244,21 @@ def test_backward_identical_keys_give_zero_dq():
         assert np.max(np.abs(dq)) <= 1e-12
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_from_saved_outputs_equals_exact_gradient(causal):
+    """Fed the exact O and LSE, the saved-output backward is the exact gradient."""
+    rng = np.random.default_rng(16)
+    q, k, v, do = _rand(rng, 40, 8), _rand(rng, 40, 8), _rand(rng, 40, 8), _rand(rng, 40, 8)
+    o, lse = orc.head_forward(q, k, v, causal=causal, scale=0.45)
+    a = orc.head_backward_from_saved(q, k, v, o, do, lse, causal=causal, scale=0.45)
+    b = orc.head_backward(q, k, v, do, causal=causal, scale=0.45)
+    for x, y in zip(a, b):
+        assert np.max(np.abs(x - y)) <= 1e-12
+    # and it really uses the given O: a shifted O changes dQ and dK but not dV
+    a2 = orc.head_backward_from_saved(q, k, v, o + 0.01, do, lse, causal=causal, scale=0.45)
+    assert np.max(np.abs(a2[0] - a[0])) > 1e-6 and np.max(np.abs(a2[2] - a[2])) <= 1e-12
+
+
 # ------------------------------------------------ tiled algorithm equivalence
 
 @pytest.mark.parametrize("tau", [0.0, 8.0, math.inf])
