@@ -54,11 +54,11 @@ def run_fwd_bwd(torch, w, qb, kb, vb, dob):
     return gu.to_f64(dq.view), gu.to_f64(dk.view), gu.to_f64(dv.view)
 
 
-def check_grads(got, ref, what):
-    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+def check_grads(got, ref, what, tols=(gu.GRAD_REL_RMS,) * 3):
+    for name, g, r, tol in zip(("dQ", "dK", "dV"), got, ref, tols):
         assert np.all(np.isfinite(g)), f"{what}: non-finite {name}"
         e = gu.rel_rms(g, r)
-        assert e <= gu.GRAD_REL_RMS, f"{what}: {name} rel-RMS {e:.3e}"
+        assert e <= tol, f"{what}: {name} rel-RMS {e:.3e} > {tol:.3e}"
 
 
 def full_compare(torch, w):
@@ -129,7 +129,29 @@ def test_stress_inputs_from_saved_outputs(torch):
     for h in range(H):
         ref = oracle.head_backward_from_saved(q[0, h], k[0, h], v[0, h], o_saved[0, h], do[0, h],
                                               lse_saved[0, h], causal=True, scale=w.scale)
-        check_grads((gu.to_f64(dq)[0, h], gu.to_f64(dk)[0, h], gu.to_f64(dv)[0, h]), ref, f"stress h{h}")
+        tols = [max(gu.GRAD_REL_RMS, 2 * 2.0 ** -9 / math.sqrt(3) * c)
+                for c in _conditioning(q[0, h], k[0, h], v[0, h], o_saved[0, h], do[0, h],
+                                       lse_saved[0, h], w.scale)]
+        check_grads((gu.to_f64(dq)[0, h], gu.to_f64(dk)[0, h], gu.to_f64(dv)[0, h]), ref,
+                    f"stress h{h}", tols)
+
+
+def _conditioning(q, k, v, o, do, lse, scale):
+    """Frobenius condition numbers ||(|A||B|)|| / ||A B|| of the three gradient products.
+
+    The kernel stores P and dS in bf16 (unit roundoff 2^-9, RMS 2^-9/sqrt(3)
+    for round-to-nearest) before the dV, dK and dQ products; the relative RMS
+    error those roundings cause grows with this ratio, which is large when
+    sum_j dS_ij nearly cancels against keys with a large common component.
+    """
+    n = q.shape[0]
+    s = scale * q @ k.T
+    s = np.where(np.tril(np.ones((n, k.shape[0]))) > 0, s, -np.inf)
+    p = np.exp(s - lse[:, None])
+    ds = p * (do @ v.T - np.sum(do * o, axis=1)[:, None])
+    def kappa(a, b):
+        return np.linalg.norm(np.abs(a) @ np.abs(b)) / np.linalg.norm(a @ b)
+    return kappa(ds, k), kappa(ds.T, q), kappa(p.T, do)
 
 
 def test_full_size_backward(torch):
