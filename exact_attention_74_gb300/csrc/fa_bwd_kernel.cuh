@@ -16,13 +16,15 @@
 //            memory, looping over the query tiles that can see its keys
 //            (causal: only tiles at or below the diagonal):
 //              warp 0    TMA producer (Q, dO tiles, LSE and D rows, 2 stages)
-//              warp 1    MMA issuer: S^T = K Q^T, dP^T = V dO^T into tensor
-//                        memory; then dV += P^T dO (P read from tensor
-//                        memory), dK += dS^T Q and the partial dQ = dS K (dS
-//                        read from shared memory in its two orientations)
-//              warps 2-5 one key row per thread: P, dS; P back into tensor
-//                        memory, dS into shared memory (128-byte swizzle)
-//              warps 6-9 drain each partial dQ from tensor memory into the
+//              warp 1    MMA issuer, per query tile i:
+//                          dQ_i = dS K (first, so its drain overlaps the rest),
+//                          dV += P^T dO, dK += dS^T Q, then for tile i+1
+//                          S^T = K Q^T and, once dQ_i is drained, dP^T = V dO^T
+//              warps 2-9 two warps per tensor-memory lane quarter (one key
+//                        row per thread), each warp of a pair on half of the
+//                        128 query columns: P back into tensor memory, dS
+//                        into shared memory (128-byte swizzle); then the same
+//                        warps drain their half of the partial dQ into the
 //                        fp32 accumulator with vector atomic adds
 //            dK and dV stay in tensor memory for the whole loop and are
 //            written once at the end.
@@ -165,14 +167,11 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int j, bh;
-  if (p.causal) {   // key tile 0 sees every query tile: run the heaviest first
-    j = static_cast<int>(blockIdx.x) / p.BH;
-    bh = static_cast<int>(blockIdx.x) % p.BH;
-  } else {
-    j = static_cast<int>(blockIdx.x) % p.n_kv_tiles;
-    bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
-  }
+  // Head-major order: the CTAs resident at one time cover only a few heads,
+  // so their fp32 dQ accumulators (and Q, dO tiles) stay in L2.  Within a
+  // head, key tile 0 runs first: with a causal mask it sees the most query tiles.
+  const int j = static_cast<int>(blockIdx.x) % p.n_kv_tiles;
+  const int bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
   const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
   const int n_it = max(0, p.n_q_tiles - i0);
 
@@ -180,12 +179,12 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(bar(C::kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kQFull + s), 1);
-      mbar_init(bar(C::kQEmpty + s), 1 + 4);   // MMA commit + one arrive per compute warp
+      mbar_init(bar(C::kQEmpty + s), 1 + 8);   // MMA commit + one arrive per compute warp
     }
     mbar_init(bar(C::kSFull), 1);
-    mbar_init(bar(C::kPFull), 128);
+    mbar_init(bar(C::kPFull), 256);
     mbar_init(bar(C::kDQFull), 1);
-    mbar_init(bar(C::kDQFree), 128);
+    mbar_init(bar(C::kDQFree), 256);
     mbar_init(bar(C::kAccFull), 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -229,32 +228,42 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       constexpr uint32_t idKV = idesc_bf16(kBM, D, false, true);
       constexpr uint32_t idQ = idesc_bf16(kBN, D, true, true);
       const uint32_t sK = sb + C::kK, sV = sb + C::kV, sDS = sb + C::kDS;
-      bool ok = mbar_wait(bar(C::kKVFull), 0, p.ctl, abort_flag);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it & 1;
-        ok = mbar_wait(bar(C::kQFull + s), (it >> 1) & 1, p.ctl, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sQ = sb + C::q_off(s), sdO = sb + C::do_off(s);
+      auto issue_S = [&](int st) {       // S^T = K Q^T
+        const uint32_t sQ = sb + C::q_off(st);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {     // S^T = K Q^T
+        for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
           mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 0, 1024), sdesc_sw128(sQ + off, 0, 1024), idS, k > 0);
         }
-        if (it > 0) {   // the partial dQ of the previous tile must be drained first
-          ok = mbar_wait(bar(C::kDQFree), (it - 1) & 1, p.ctl, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-        }
+      };
+      auto issue_dP = [&](int st) {      // dP^T = V dO^T
+        const uint32_t sdO = sb + C::do_off(st);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {     // dP^T = V dO^T
+        for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
           mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 0, 1024), sdesc_sw128(sdO + off, 0, 1024), idS, k > 0);
         }
+      };
+      bool ok = mbar_wait(bar(C::kKVFull), 0, p.ctl, abort_flag);
+      if (ok) ok = mbar_wait(bar(C::kQFull + 0), 0, p.ctl, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+        issue_dP(0);
         tc_commit(bar(C::kSFull));
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it & 1;
+        const uint32_t sQ = sb + C::q_off(s), sdO = sb + C::do_off(s);
         ok = mbar_wait(bar(C::kPFull), it & 1, p.ctl, abort_flag);
         if (!ok) break;
         tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k) {   // dQ_i = dS K  (unscaled partial)
+          mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + k * 2048, kPanel, 1024),
+                 sdesc_sw128(sK + k * 2048, kPanel, 1024), idQ, k > 0);
+        }
+        tc_commit(bar(C::kDQFull));
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {   // dV += P^T dO
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k, sdesc_sw128(sdO + k * 2048, kPanel, 1024), idKV,
@@ -265,24 +274,32 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
                  sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int k = 0; k < kBM / 16; ++k) {   // dQ_i = dS K  (unscaled partial)
-          mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + k * 2048, kPanel, 1024),
-                 sdesc_sw128(sK + k * 2048, kPanel, 1024), idQ, k > 0);
-        }
-        tc_commit(bar(C::kDQFull));
         tc_commit(bar(C::kQEmpty + s));
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) & 1;
+          ok = mbar_wait(bar(C::kQFull + s1), ((it + 1) >> 1) & 1, p.ctl, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_S(s1);
+          ok = mbar_wait(bar(C::kDQFree), it & 1, p.ctl, abort_flag);   // dQ_i drained
+          if (!ok) break;
+          tc_fence_after();
+          issue_dP(s1);
+          tc_commit(bar(C::kSFull));
+        }
       }
       if (ok) tc_commit(bar(C::kAccFull));
     }
-  } else if (warp >= 2 && warp < 6) {
-    // ------------------------------------------------------- P and dS rows
-    const int rank = warp & 3;
-    const int r = rank * 32 + lane;          // key row within the tile
+  } else if (warp >= 2) {
+    // ------------------------------------------ P and dS rows, dQ drainage
+    const int rank = warp & 3;               // tensor-memory lane quarter
+    const int half = (warp - 2) >> 2;        // query columns [64 half, 64 half + 64)
+    const int r = rank * 32 + lane;          // key row (and dQ query row) within the tile
     const int kg = j * kBM + r;              // global key index
     const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
     const bool key_ok = kg < p.N_kv;
     const float2 c2 = make_float2(p.c, p.c);
+    const uint32_t pair_bar = 1 + rank;      // named barrier of the two warps of this lane quarter
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
@@ -296,11 +313,17 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const float* dlt_s = reinterpret_cast<const float*>(smem + C::dlt_off(s));
       // queries q with q_g < k_g are masked (causal); only the diagonal tile has any
       const int lim = (p.causal && i == j) ? r : 0;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      uint32_t pk_keep[2][16];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * half + cc;        // 32-query chunk
         uint32_t sv[32], dp[32];
         tmem_ld_x32(tmem + lane_addr + C::kColS + 32 * ch, sv);
         tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, dp);
+        // P of chunk ch lands on the S columns of queries [16 ch, 16 ch + 16),
+        // which the first warp of the pair reads in its second chunk: it
+        // signals once those reads are done, the second warp writes after.
+        if (half == 0 && cc == 1) named_bar_arrive(pair_bar, 64);
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
@@ -322,7 +345,12 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             dk[q >> 1] = pack_bf16x2(ds.x, ds.y);
           }
         }
-        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * ch, pk);
+        if (half == 0) {
+          tmem_st_x16(tmem + lane_addr + C::kColS + 16 * ch, pk);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) pk_keep[cc][u] = pk[u];
+        }
         // dS^T row r, queries 32ch..32ch+31: panel ch/2, 16-byte chunks (ch&1)*4 + u
         uint8_t* rowp = smem + C::kDS + (ch >> 1) * kPanel + r * 128;
 #pragma unroll
@@ -332,11 +360,35 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
+      if (half == 1) {
+        named_bar_sync(pair_bar, 64);
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 2, pk_keep[0]);
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 3, pk_keep[1]);
+      }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::kPFull));
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::kQEmpty + s));
+      // ---- drain this warp's half of the partial dQ (rows = queries of tile i)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), it & 1, p.ctl, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int qg = i * kBN + r;
+      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.N_q + qg) * D + half * (D / 2);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_addr + C::kColDP + half * (D / 2) + 32 * ch, v);
+        if (qg < p.N_q) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + 32 * ch + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                       __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kDQFree));
     }
     // ----------------------------------------------------- dK, dV epilogue
     bool ready = ok;
@@ -344,14 +396,14 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     ready = __all_sync(0xffffffffu, ready);
     if (n_it == 0 || ready) {
       if (n_it > 0) tc_fence_after();
-      const size_t rowoff = (static_cast<size_t>(bh) * p.N_kv + kg) * D;
+      const size_t rowoff = (static_cast<size_t>(bh) * p.N_kv + kg) * D + half * (D / 2);
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* outp = (which == 0 ? p.dv : p.dk) + rowoff;
         const float f = which == 0 ? 1.f : p.scale;
-        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+        const uint32_t col = (which == 0 ? C::kColDV : C::kColDK) + half * (D / 2);
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = 0; ch < D / 64; ++ch) {
           uint32_t v[32];
           if (n_it > 0) {
             tmem_ld_x32(tmem + lane_addr + col + 32 * ch, v);
@@ -372,31 +424,6 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           }
         }
       }
-    }
-  } else if (n_it > 0 && warp >= 6) {
-    // -------------------------------------------------------- dQ drainage
-    const int rank = warp & 3;
-    const int r = rank * 32 + lane;          // query row within the tile
-    const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
-    for (int it = 0; it < n_it; ++it) {
-      const int qg = (i0 + it) * kBN + r;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), it & 1, p.ctl, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.N_q + qg) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, v);
-        if (qg < p.N_q) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + 32 * ch + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                       __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kDQFree));
     }
   }
 

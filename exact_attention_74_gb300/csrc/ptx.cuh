@@ -127,6 +127,15 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Named CTA barrier `id` (1..15) over `count` threads (a multiple of 32):
+// arrive without waiting, or arrive and wait.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("barrier.cta.arrive.aligned %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("barrier.cta.sync.aligned %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
 // Four fp32 atomic additions to consecutive addresses (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
