@@ -16,16 +16,18 @@
 //            memory, looping over the query tiles that can see its keys
 //            (causal: only tiles at or below the diagonal):
 //              warp 0    TMA producer (Q, dO tiles, LSE and D rows, 2 stages)
-//              warp 1    MMA issuer, per query tile i:
-//                          dQ_i = dS K (first, so its drain overlaps the rest),
-//                          dV += P^T dO, dK += dS^T Q, then for tile i+1
-//                          S^T = K Q^T and, once dQ_i is drained, dP^T = V dO^T
+//              warp 1    MMA issuer, per query tile i, in this order:
+//                          dQ_i = dS K, dV += P^T dO, S^T_{i+1} = K Q^T_{i+1},
+//                          dK += dS^T Q, dP^T_{i+1} = V dO^T_{i+1}
+//                        so the drain of dQ_i and the P of tile i+1 overlap
+//                        the products that follow them
 //              warps 2-9 two warps per tensor-memory lane quarter (one key
 //                        row per thread), each warp of a pair on half of the
-//                        128 query columns: P back into tensor memory, dS
-//                        into shared memory (128-byte swizzle); then the same
-//                        warps drain their half of the partial dQ into the
-//                        fp32 accumulator with vector atomic adds
+//                        128 query columns: P (as soon as S is ready) back
+//                        into tensor memory, then dS (once dP is ready) into
+//                        shared memory (128-byte swizzle); then the same warps
+//                        drain their half of the partial dQ into the fp32
+//                        accumulator with vector atomic adds
 //            dK and dV stay in tensor memory for the whole loop and are
 //            written once at the end.
 //   convert -- dQ = bf16(scale * accumulator).
@@ -58,7 +60,7 @@ struct Cfg {
   static constexpr int kBar = kDS + 2 * kPanel;
   // barrier indices
   static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
-                       kDQFree = 8, kAccFull = 9, kNumBars = 10;
+                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kNumBars = 11;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmem = kMisc + 16;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -182,6 +184,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       mbar_init(bar(C::kQEmpty + s), 1 + 8);   // MMA commit + one arrive per compute warp
     }
     mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kDPFull), 1);
     mbar_init(bar(C::kPFull), 256);
     mbar_init(bar(C::kDQFull), 1);
     mbar_init(bar(C::kDQFree), 256);
@@ -249,12 +252,15 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       if (ok) {
         tc_fence_after();
         issue_S(0);
-        issue_dP(0);
         tc_commit(bar(C::kSFull));
+        issue_dP(0);
+        tc_commit(bar(C::kDPFull));
       }
       for (int it = 0; it < n_it && ok; ++it) {
         const int s = it & 1;
         const uint32_t sQ = sb + C::q_off(s), sdO = sb + C::do_off(s);
+        const bool next = it + 1 < n_it;
+        const int s1 = (it + 1) & 1;
         ok = mbar_wait(bar(C::kPFull), it & 1, p.ctl, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -269,23 +275,25 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k, sdesc_sw128(sdO + k * 2048, kPanel, 1024), idKV,
                  (it > 0 || k > 0) ? 1u : 0u);
         }
+        if (next) {                             // S of the next tile (P_i has been consumed)
+          ok = mbar_wait(bar(C::kQFull + s1), ((it + 1) >> 1) & 1, p.ctl, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_S(s1);
+          tc_commit(bar(C::kSFull));
+        }
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {   // dK += dS^T Q  (unscaled)
           mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
                  sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(bar(C::kQEmpty + s));
-        if (it + 1 < n_it) {
-          const int s1 = (it + 1) & 1;
-          ok = mbar_wait(bar(C::kQFull + s1), ((it + 1) >> 1) & 1, p.ctl, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_S(s1);
-          ok = mbar_wait(bar(C::kDQFree), it & 1, p.ctl, abort_flag);   // dQ_i drained
+        if (next) {                             // dP of the next tile once dQ_i is drained
+          ok = mbar_wait(bar(C::kDQFree), it & 1, p.ctl, abort_flag);
           if (!ok) break;
           tc_fence_after();
           issue_dP(s1);
-          tc_commit(bar(C::kSFull));
+          tc_commit(bar(C::kDPFull));
         }
       }
       if (ok) tc_commit(bar(C::kAccFull));
@@ -311,45 +319,74 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       tc_fence_after();
       const float* lse_s = reinterpret_cast<const float*>(smem + C::lse_off(s));
       const float* dlt_s = reinterpret_cast<const float*>(smem + C::dlt_off(s));
-      // queries q with q_g < k_g are masked (causal); only the diagonal tile has any
+      // queries q with q_g < k_g are masked (causal); only the diagonal tile has
+      // any, and only the last key tile has keys past N_kv
       const int lim = (p.causal && i == j) ? r : 0;
+      const bool masked = __any_sync(0xffffffffu, lim > 0 || !key_ok);
+      // ---- P = 2^(S c - LSE log2 e), as soon as S is ready
+      float pf[2][32];
       uint32_t pk_keep[2][16];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int ch = 2 * half + cc;        // 32-query chunk
-        uint32_t sv[32], dp[32];
+        uint32_t sv[32];
         tmem_ld_x32(tmem + lane_addr + C::kColS + 32 * ch, sv);
-        tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, dp);
         // P of chunk ch lands on the S columns of queries [16 ch, 16 ch + 16),
         // which the first warp of the pair reads in its second chunk: it
         // signals once those reads are done, the second warp writes after.
         if (half == 0 && cc == 1) named_bar_arrive(pair_bar, 64);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * ch + u);
-          const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + 32 * ch + u);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int q = u + 2 * h;          // column within the chunk
+            const int q = u + 2 * h;
             const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
             const float2 x = fma2(make_float2(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1])), c2, nl);
-            float p0 = ex2_hw(x.x), p1 = ex2_hw(x.y);
-            const int qc = 32 * ch + q;
-            if (!key_ok || qc < lim) p0 = 0.f;
-            if (!key_ok || qc + 1 < lim) p1 = 0.f;
-            const float2 t = add2(make_float2(__uint_as_float(dp[q]), __uint_as_float(dp[q + 1])), nd);
-            const float2 ds = mul2(make_float2(p0, p1), t);
-            pk[q >> 1] = pack_bf16x2(p0, p1);
-            dk[q >> 1] = pack_bf16x2(ds.x, ds.y);
+            pf[cc][q] = ex2_hw(x.x);
+            pf[cc][q + 1] = ex2_hw(x.y);
           }
         }
+        if (masked) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            if (!key_ok || 32 * ch + q < lim) pf[cc][q] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) pk[q >> 1] = pack_bf16x2(pf[cc][q], pf[cc][q + 1]);
         if (half == 0) {
           tmem_st_x16(tmem + lane_addr + C::kColS + 16 * ch, pk);
         } else {
 #pragma unroll
           for (int u = 0; u < 16; ++u) pk_keep[cc][u] = pk[u];
+        }
+      }
+      if (half == 1) {
+        named_bar_sync(pair_bar, 64);
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 2, pk_keep[0]);
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 3, pk_keep[1]);
+      }
+      // ---- dS = P o (dP - D), once dP is ready
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDPFull), it & 1, p.ctl, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * half + cc;
+        uint32_t dp[32], dk[16];
+        tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, dp);
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + 32 * ch + u);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q = u + 2 * h;
+            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+            const float2 t = add2(make_float2(__uint_as_float(dp[q]), __uint_as_float(dp[q + 1])), nd);
+            const float2 ds = mul2(make_float2(pf[cc][q], pf[cc][q + 1]), t);
+            dk[q >> 1] = pack_bf16x2(ds.x, ds.y);
+          }
         }
         // dS^T row r, queries 32ch..32ch+31: panel ch/2, 16-byte chunks (ch&1)*4 + u
         uint8_t* rowp = smem + C::kDS + (ch >> 1) * kPanel + r * 128;
@@ -359,11 +396,6 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           *reinterpret_cast<uint4*>(rowp + chunk * 16) =
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
-      }
-      if (half == 1) {
-        named_bar_sync(pair_bar, 64);
-        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 2, pk_keep[0]);
-        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 3, pk_keep[1]);
       }
       fence_async_smem();
       tc_fence_before();
@@ -388,7 +420,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(C::kDQFree));
+      mbar_arrive_relaxed(bar(C::kDQFree));   // the reads are complete; the atomics need not be
     }
     // ----------------------------------------------------- dK, dV epilogue
     bool ready = ok;
