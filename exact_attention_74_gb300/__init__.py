@@ -19,6 +19,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_UNSUPPORTED", "FA_ERR_ALIGN", "FA_ERR_WORKSPACE",
     "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FAError", "library", "library_path",
     "fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_last_device_status",
+    "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE",
     "fa_set_wait_timeout_ns", "fa_status_string", "fa_test_exp2", "fa_test_mma_tile",
     "fa_test_wait_timeout", "forward", "backward", "EXPORTED_SYMBOLS",
 ]
@@ -40,6 +41,8 @@ _SIGNATURES = {
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                     _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_get_last_device_status": (_i, [_vp]),
     "fa_set_wait_timeout_ns": (_i, [_ull]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
@@ -95,6 +98,16 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
            workspace, workspace_bytes, stream=0):
     return _call("fa_bwd", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
                  workspace, workspace_bytes, stream)
+
+
+# Bytes of scratch fa_bwd_noalloc can use (FA_BWD_NOALLOC_MAX_WORKSPACE in fa.h).
+FA_BWD_NOALLOC_MAX_WORKSPACE = 16 << 20
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, stream=0):
+    """fa_bwd without a workspace argument, for callers that cannot allocate device memory."""
+    return _call("fa_bwd_noalloc", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal,
+                 scale, stream)
 
 
 def fa_get_last_device_status(stream=0):

@@ -110,6 +110,40 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
            void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
+ *
+ * (The pages describe no such call; it is an interface convenience.)  Some
+ * callers have no way to obtain a workspace: code embedded in a host
+ * framework that hands it only the input and output buffers, servers that
+ * forbid allocation on the request path because cudaMalloc can fail under
+ * memory pressure and cudaFree synchronises the whole device, or processes
+ * whose device memory is reserved up front.  This entry point takes the same
+ * arguments as fa_bwd without the workspace and uses scratch memory the
+ * library reserves in device memory when it is loaded:
+ * FA_BWD_NOALLOC_MAX_WORKSPACE bytes on every GPU that loads the library,
+ * held until the process exits.  It allocates nothing.
+ *
+ *   - Problems whose fa_bwd_workspace_bytes(...) exceeds
+ *     FA_BWD_NOALLOC_MAX_WORKSPACE return FA_ERR_WORKSPACE and launch nothing
+ *     (at d = 128 that is about 32,000 query rows B*H*N_q; use fa_bwd with a
+ *     workspace of your own beyond that).  Other argument errors are those
+ *     of fa_bwd.
+ *   - The first call on a device looks up the scratch's device address with
+ *     that device current (a CUDA runtime query, no allocation); make that
+ *     first call before any stream capture on that device.
+ *   - Every call on a device shares the one scratch area.  Each call clears
+ *     what it needs before using it, but calls that can overlap on the GPU
+ *     (for example on two streams without ordering between them) race on it
+ *     and give wrong results: order such calls, or use fa_bwd.
+ */
+#define FA_BWD_NOALLOC_MAX_WORKSPACE ((size_t)16 << 20)
+
+int fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                   int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+                   fa_stream_t stream);
+
+/*
  * fa_get_last_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns FA_OK, FA_ERR_TIMEOUT if
  * a bounded wait in any kernel of this library ran out since the last call,
