@@ -110,6 +110,23 @@ int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D map over a contiguous fp32 [BH, N, d] tensor: box box_cols x box_rows
+// x 1 with 128-byte swizzle (box_cols * 4 must be 128); rows past N are
+// skipped by stores and reductions.
+int make_map_f32(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 constexpr int kDefaultEmuPer32 = 0;
 constexpr float kDefaultTau = 8.0f;
 
@@ -191,6 +208,7 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmdO, dO, d, N_q, BH)) != FA_OK) return st;
+  if ((st = make_map_f32(&a.tmDQ, workspace, d, N_q, BH, 32, 32)) != FA_OK) return st;
   const size_t rows = static_cast<size_t>(BH) * N_q;
   a.o = O;
   a.dO = dO;

@@ -15,19 +15,24 @@
 //   main  -- one CTA per (128-key tile, batch*head), K and V resident in shared
 //            memory, looping over the query tiles that can see its keys
 //            (causal: only tiles at or below the diagonal):
-//              warp 0    TMA producer (Q, dO tiles, LSE and D rows, 2 stages)
+//              warp 0    TMA producer (Q, dO tiles, LSE and D rows, 2 stages);
+//                        before refilling a stage it issues the TMA reduce-adds
+//                        of the dQ partial the compute warps staged there
 //              warp 1    MMA issuer, per query tile i, in this order:
-//                          dQ_i = dS K, dV += P^T dO, S^T_{i+1} = K Q^T_{i+1},
-//                          dK += dS^T Q, dP^T_{i+1} = V dO^T_{i+1}
-//                        so the drain of dQ_i and the P of tile i+1 overlap
-//                        the products that follow them
+//                          dQ_i = dS K, dK += dS^T Q, dV += P^T dO,
+//                          S^T_{i+1} = K Q^T_{i+1}, dP^T_{i+1} = V dO^T_{i+1}
+//                        so that once dV is issued tile i's Q and dO are dead
+//                        and the drain of dQ_i and the P of tile i+1 overlap
+//                        the products that follow
 //              warps 2-9 two warps per tensor-memory lane quarter (one key
 //                        row per thread), each warp of a pair on half of the
 //                        128 query columns: P (as soon as S is ready) back
 //                        into tensor memory, then dS (once dP is ready) into
 //                        shared memory (128-byte swizzle); then the same warps
-//                        drain their half of the partial dQ into the fp32
-//                        accumulator with vector atomic adds
+//                        drain their half of the partial dQ: tensor memory ->
+//                        registers -> tile i's dead Q/dO buffers in the TMA
+//                        layout, handed to the producer, which adds it into
+//                        the fp32 accumulator with TMA reduce-adds
 //            dK and dV stay in tensor memory for the whole loop and are
 //            written once at the end.
 //   convert -- dQ = bf16(scale * accumulator).
@@ -59,7 +64,7 @@ struct Cfg {
   static constexpr int kDS = kStage0 + 2 * kStageBytes;   // dS^T tile, 2 panels of 128 keys x 64 queries
   static constexpr int kBar = kDS + 2 * kPanel;
   // barrier indices
-  static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
+  static constexpr int kKVFull = 0, kQFull = 1, kStaged = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
                        kDQFree = 8, kAccFull = 9, kDPFull = 10, kNumBars = 11;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmem = kMisc + 16;
@@ -155,7 +160,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-            const Params p) {
+            const __grid_constant__ CUtensorMap tmDQ, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
@@ -181,7 +186,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(bar(C::kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kQFull + s), 1);
-      mbar_init(bar(C::kQEmpty + s), 1 + 8);   // MMA commit + one arrive per compute warp
+      mbar_init(bar(C::kStaged + s), 8);       // one arrive per compute warp once its dQ boxes are staged
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kDPFull), 1);
@@ -209,10 +214,25 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tma_load_3d(sb + C::kV + pn * kPanel, &tmV, bar(C::kKVFull), pn * 64, j * kBM, bh);
       }
       const uint64_t keep = l2_policy_evict_last();
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        if (!mbar_wait(bar(C::kQEmpty + s), ((it >> 1) & 1) ^ 1, p.ctl, abort_flag)) break;
-        const int i = i0 + it;
+      constexpr int kBoxes = D / 64;            // 32-column boxes per compute warp
+      for (int t = 0; t < n_it + 2; ++t) {
+        const int s = t & 1;
+        if (t >= 2) {
+          // Tile t-2 staged its partial dQ in stage s (its Q and dO were no
+          // longer read): add it into the accumulator, and once the staging
+          // has been read the stage is free for tile t.
+          if (!mbar_wait(bar(C::kStaged + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
+          const int ip = i0 + t - 2;
+          for (int hf = 0; hf < 2; ++hf)
+            for (int c = 0; c < kBoxes; ++c)
+              for (int rk = 0; rk < 4; ++rk)
+                tma_reduce_add_3d(&tmDQ, sb + C::q_off(s) + ((hf * kBoxes + c) * 4 + rk) * 4096,
+                                  hf * (D / 2) + 32 * c, ip * kBN + rk * 32, bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        if (t >= n_it) continue;
+        const int i = i0 + t;
         const uint32_t fb = bar(C::kQFull + s);
         mbar_arrive_expect_tx(fb, 2 * C::kTile + 1024);
         for (int pn = 0; pn < D / 64; ++pn) {
@@ -223,6 +243,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         bulk_load(sb + C::lse_off(s), p.lse2 + row, 512, fb);
         bulk_load(sb + C::dlt_off(s), p.delta + row, 512, fb);
       }
+      bulk_wait_group0();                       // every reduction has landed
     }
   } else if (n_it > 0 && warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -269,12 +290,19 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + k * 2048, kPanel, 1024),
                  sdesc_sw128(sK + k * 2048, kPanel, 1024), idQ, k > 0);
         }
-        tc_commit(bar(C::kDQFull));
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {   // dK += dS^T Q  (unscaled)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
+                 sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        }
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {   // dV += P^T dO
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k, sdesc_sw128(sdO + k * 2048, kPanel, 1024), idKV,
                  (it > 0 || k > 0) ? 1u : 0u);
         }
+        // dQ_i is ready and this stage's Q and dO are no longer read: the
+        // drain may stage dQ_i in them
+        tc_commit(bar(C::kDQFull));
         if (next) {                             // S of the next tile (P_i has been consumed)
           ok = mbar_wait(bar(C::kQFull + s1), ((it + 1) >> 1) & 1, p.ctl, abort_flag);
           if (!ok) break;
@@ -282,12 +310,6 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           issue_S(s1);
           tc_commit(bar(C::kSFull));
         }
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {   // dK += dS^T Q  (unscaled)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
-                 sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(C::kQEmpty + s));
         if (next) {                             // dP of the next tile once dQ_i is drained
           ok = mbar_wait(bar(C::kDQFree), it & 1, p.ctl, abort_flag);
           if (!ok) break;
@@ -400,27 +422,33 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::kPFull));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kQEmpty + s));
       // ---- drain this warp's half of the partial dQ (rows = queries of tile i)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), it & 1, p.ctl, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const int qg = i * kBN + r;
-      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.N_q + qg) * D + half * (D / 2);
-#pragma unroll 1
-      for (int ch = 0; ch < D / 64; ++ch) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_addr + C::kColDP + half * (D / 2) + 32 * ch, v);
-        if (qg < p.N_q) {
+      constexpr int kBoxes = D / 64;          // 32-column boxes per warp
+      uint32_t v[kBoxes][32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + 32 * ch + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                       __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-        }
-      }
+      for (int c = 0; c < kBoxes; ++c)
+        tmem_ld_x32(tmem + lane_addr + C::kColDP + half * (D / 2) + 32 * c, v[c]);
       tc_fence_before();
-      mbar_arrive_relaxed(bar(C::kDQFree));   // the reads are complete; the atomics need not be
+      mbar_arrive_relaxed(bar(C::kDQFree));   // the tensor-memory reads are complete
+      // Stage each 32-row x 32-column fp32 box in tile i's dead Q/dO buffers,
+      // laid out as TMA's 128-byte swizzle expects (row = lane, 16-byte chunk
+      // j at j ^ (row & 7)); the producer adds the boxes into the accumulator.
+      const uint32_t stage = sb + C::q_off(s);
+#pragma unroll
+      for (int c = 0; c < kBoxes; ++c) {
+        const uint32_t box = stage + ((half * kBoxes + c) * 4 + rank) * 4096;
+        uint8_t* rowp = smem + (box - sb) + lane * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (lane & 7)) * 16)) =
+              make_uint4(v[c][4 * u], v[c][4 * u + 1], v[c][4 * u + 2], v[c][4 * u + 3]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kStaged + s));   // the producer reduces it
     }
     // ----------------------------------------------------- dK, dV epilogue
     bool ready = ok;
@@ -503,7 +531,7 @@ cudaError_t launch(const BwdLaunch& a) {
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_kv_tiles) * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmem, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmem, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.tmDQ, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long n8 = static_cast<long long>(a.BH) * a.N_q * D / 8;

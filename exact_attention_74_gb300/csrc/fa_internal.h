@@ -26,6 +26,7 @@ cudaError_t launch_fwd_d128(const FwdLaunch& a);
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO;   // same map shape as the forward's
+  CUtensorMap tmDQ;                  // fp32 dQ accumulator (d, N_q, B*H), 32 x 32 x 1 boxes
   const void* o;
   const void* dO;
   const float* lse;
@@ -45,5 +46,6 @@ cudaError_t launch_bwd(const BwdLaunch& a);
 // Defined in fa_api.cu.
 int device_ctl(DevCtl* ctl);
 int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows = 128);
+int make_map_f32(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_cols, int box_rows);
 
 }  // namespace fa
