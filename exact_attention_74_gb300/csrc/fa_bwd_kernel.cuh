@@ -65,7 +65,7 @@ struct Cfg {
   static constexpr int kBar = kDS + 2 * kPanel;
   // barrier indices
   static constexpr int kKVFull = 0, kQFull = 1, kStaged = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
-                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kNumBars = 11;
+                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kDOFull = 11, kNumBars = 13;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmem = kMisc + 16;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -185,7 +185,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::kQFull + s), 1);
+      mbar_init(bar(C::kQFull + s), 1);      // Q tile + LSE and D rows
+      mbar_init(bar(C::kDOFull + s), 1);     // dO tile
       mbar_init(bar(C::kStaged + s), 8);       // one arrive per compute warp once its dQ boxes are staged
     }
     mbar_init(bar(C::kSFull), 1);
@@ -219,29 +220,34 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const int s = t & 1;
         if (t >= 2) {
           // Tile t-2 staged its partial dQ in stage s (its Q and dO were no
-          // longer read): add it into the accumulator, and once the staging
-          // has been read the stage is free for tile t.
+          // longer read): add it into the accumulator in two groups, the
+          // boxes held in the Q buffer first, and refill each buffer as soon
+          // as its boxes have been read.
           if (!mbar_wait(bar(C::kStaged + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
           const int ip = i0 + t - 2;
-          for (int hf = 0; hf < 2; ++hf)
+          for (int hf = 0; hf < 2; ++hf) {
             for (int c = 0; c < kBoxes; ++c)
               for (int rk = 0; rk < 4; ++rk)
                 tma_reduce_add_3d(&tmDQ, sb + C::q_off(s) + ((hf * kBoxes + c) * 4 + rk) * 4096,
                                   hf * (D / 2) + 32 * c, ip * kBN + rk * 32, bh);
-          bulk_commit_group();
-          bulk_wait_group_read0();
+            bulk_commit_group();
+          }
         }
         if (t >= n_it) continue;
         const int i = i0 + t;
-        const uint32_t fb = bar(C::kQFull + s);
-        mbar_arrive_expect_tx(fb, 2 * C::kTile + 1024);
-        for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d_hint(sb + C::q_off(s) + pn * kPanel, &tmQ, fb, pn * 64, i * kBN, bh, keep);
-          tma_load_3d_hint(sb + C::do_off(s) + pn * kPanel, &tmdO, fb, pn * 64, i * kBN, bh, keep);
-        }
+        if (t >= 2) bulk_wait_group_read<1>();    // Q-buffer boxes read
+        const uint32_t fq = bar(C::kQFull + s);
+        mbar_arrive_expect_tx(fq, C::kTile + 1024);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d_hint(sb + C::q_off(s) + pn * kPanel, &tmQ, fq, pn * 64, i * kBN, bh, keep);
         const size_t row = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * kBN;
-        bulk_load(sb + C::lse_off(s), p.lse2 + row, 512, fb);
-        bulk_load(sb + C::dlt_off(s), p.delta + row, 512, fb);
+        bulk_load(sb + C::lse_off(s), p.lse2 + row, 512, fq);
+        bulk_load(sb + C::dlt_off(s), p.delta + row, 512, fq);
+        if (t >= 2) bulk_wait_group_read<0>();    // dO-buffer boxes read
+        const uint32_t fd = bar(C::kDOFull + s);
+        mbar_arrive_expect_tx(fd, C::kTile);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d_hint(sb + C::do_off(s) + pn * kPanel, &tmdO, fd, pn * 64, i * kBN, bh, keep);
       }
       bulk_wait_group0();                       // every reduction has landed
     }
@@ -274,6 +280,10 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tc_fence_after();
         issue_S(0);
         tc_commit(bar(C::kSFull));
+        ok = mbar_wait(bar(C::kDOFull + 0), 0, p.ctl, abort_flag);
+      }
+      if (ok) {
+        tc_fence_after();
         issue_dP(0);
         tc_commit(bar(C::kDPFull));
       }
@@ -311,7 +321,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           tc_commit(bar(C::kSFull));
         }
         if (next) {                             // dP of the next tile once dQ_i is drained
-          ok = mbar_wait(bar(C::kDQFree), it & 1, p.ctl, abort_flag);
+          ok = mbar_wait(bar(C::kDOFull + s1), ((it + 1) >> 1) & 1, p.ctl, abort_flag);
+          if (ok) ok = mbar_wait(bar(C::kDQFree), it & 1, p.ctl, abort_flag);
           if (!ok) break;
           tc_fence_after();
           issue_dP(s1);

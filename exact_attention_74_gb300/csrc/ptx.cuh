@@ -130,9 +130,11 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Wait until the shared-memory sources of this thread's bulk groups have been read.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Wait until the shared-memory sources of all but the N most recent bulk
+// groups of this thread have been read.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
 }
 // Wait until this thread's bulk groups have fully completed.
 __device__ __forceinline__ void bulk_wait_group0() {
