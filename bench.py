@@ -356,6 +356,9 @@ def run_gpu(args):
         "wall_s_timed_region": wall,
         "clocks": clocks.summary(),
     }
+    if has_bwd:
+        line["bwd_deterministic_tflops"] = deterministic_bwd_tflops(torch, fa, w, q, k, v, o, do, lse,
+                                                                    dq, dk, dv, ws, ws_bytes, stream)
     if args.sweep:
         line["sweep"] = sweep(torch, fa, dev, sh)
     if rank == 0 and not args.no_cpu_baseline:
@@ -371,11 +374,35 @@ def run_gpu(args):
     return 0
 
 
+def deterministic_bwd_tflops(torch, fa, w, q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, stream, reps=20):
+    """Backward TFLOPS of fa_bwd_ex in its fixed-order (bit-reproducible) mode."""
+    sh = stream.cuda_stream
+
+    def call():
+        st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N_q,
+                          w.N_kv, w.d, int(w.causal), w.scale, 1, ws.data_ptr(), ws_bytes, sh)
+        if st != fa.FA_OK:
+            raise fa.FAError(st, "fa_bwd_ex")
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return w.bwd_flops() / (e0.elapsed_time(e1) / reps * 1e-3) / 1e12
+
+
 def sweep(torch, fa, dev, sh, reps=10):
     """Forward TFLOPS over the 16k-token sequence sweep and the 4k / 8k configs."""
     out = []
     wls = fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True)
     wls += [fa_inputs.WORKLOADS["stress_8k"]]
+    wls += [fa_inputs.Workload("hdim64_8k", 2, 16, 8192, 8192, 64, False, 0.125, 20266),
+            fa_inputs.Workload("hdim64_8k_causal", 2, 16, 8192, 8192, 64, True, 0.125, 20266)]
     for w in wls:
         qb, kb, vb = fa_inputs.make_qkv(w)
         q, k, v = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb))
@@ -397,9 +424,36 @@ def sweep(torch, fa, dev, sh, reps=10):
         e1.record()
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / reps
-        out.append({"workload": w.name, "B": w.B, "N": w.N_q, "causal": w.causal, "ms": ms,
+        out.append({"workload": w.name, "B": w.B, "N": w.N_q, "d": w.d, "causal": w.causal, "ms": ms,
                     "tflops": w.fwd_flops() / (ms * 1e-3) / 1e12})
         del q, k, v, o, lse
+    # the backward workload: B2 H16 N8192 d128 causal, both reduction orders
+    w = fa_inputs.WORKLOADS["bwd_8k"]
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb, dob))
+    o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    for det in (0, 1):
+        def call():
+            st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N_q,
+                              w.N_kv, w.d, 1, w.scale, det, ws.data_ptr(), ws_bytes, sh)
+            assert st == fa.FA_OK
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        out.append({"workload": "bwd_8k" + ("_deterministic" if det else ""), "B": w.B, "N": w.N_q, "d": w.d,
+                    "causal": True, "ms": ms, "tflops": w.bwd_flops() / (ms * 1e-3) / 1e12})
     return out
 
 

@@ -19,7 +19,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_UNSUPPORTED", "FA_ERR_ALIGN", "FA_ERR_WORKSPACE",
     "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FAError", "library", "library_path",
     "fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_last_device_status",
-    "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE",
+    "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE", "fa_bwd_ex",
     "fa_set_wait_timeout_ns", "fa_status_string", "fa_test_exp2", "fa_test_mma_tile",
     "fa_test_wait_timeout", "forward", "backward", "EXPORTED_SYMBOLS",
 ]
@@ -41,6 +41,8 @@ _SIGNATURES = {
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                     _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                       _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_get_last_device_status": (_i, [_vp]),
@@ -98,6 +100,12 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
            workspace, workspace_bytes, stream=0):
     return _call("fa_bwd", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
                  workspace, workspace_bytes, stream)
+
+
+def fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
+              deterministic, workspace, workspace_bytes, stream=0):
+    return _call("fa_bwd_ex", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
+                 deterministic, workspace, workspace_bytes, stream)
 
 
 # Bytes of scratch fa_bwd_noalloc can use (FA_BWD_NOALLOC_MAX_WORKSPACE in fa.h).
@@ -177,7 +185,8 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None,
     return out, lse
 
 
-def backward(q, k, v, o, do, lse, causal=False, scale=None, stream=None, workspace=None):
+def backward(q, k, v, o, do, lse, causal=False, scale=None, stream=None, workspace=None,
+             deterministic=False):
     """dQ, dK, dV for bf16 tensors [B, H, N, d] and fp32 LSE [B, H, N_q]."""
     import torch
     B, H, N_q, d = q.shape
@@ -189,10 +198,10 @@ def backward(q, k, v, o, do, lse, causal=False, scale=None, stream=None, workspa
     need = fa_bwd_workspace_bytes(B, H, N_q, N_kv, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                B, H, N_q, N_kv, d, int(causal), scale, workspace.data_ptr(),
-                workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    st = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                   B, H, N_q, N_kv, d, int(causal), scale, int(deterministic), workspace.data_ptr(),
+                   workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv

@@ -184,15 +184,17 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
   const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(N_q) + 127) / 128 * 128);
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
   const size_t vec = (rows_pad * sizeof(float) + 255) / 256 * 256;
-  return acc + 2 * vec;
+  const size_t cnt = (rows_pad / 128 * sizeof(unsigned) + 255) / 256 * 256;
+  return acc + 2 * vec + cnt;
 }
 
-int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-           void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
-           void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+              void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+              int deterministic, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID;
   int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
   if (st != FA_OK) return st;
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID;
   if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
       misaligned(dO, 16) || misaligned(dQ, 16) || misaligned(dK, 16) || misaligned(dV, 16) ||
       misaligned(LSE, 4))
@@ -216,9 +218,13 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   a.dq = dQ;
   a.dk = dK;
   a.dv = dV;
+  const size_t rows_pad = static_cast<size_t>(BH) * ((static_cast<size_t>(N_q) + 127) / 128 * 128);
   a.dq_acc = static_cast<float*>(workspace);
   a.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                      (rows * d * sizeof(float) + 255) / 256 * 256);
+  a.counters = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(a.delta) +
+                                           2 * ((rows_pad * sizeof(float) + 255) / 256 * 256));
+  a.deterministic = deterministic;
   a.BH = BH;
   a.N_q = N_q;
   a.N_kv = N_kv;
@@ -232,6 +238,13 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
     return FA_ERR_CUDA;
   }
   return FA_OK;
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+           void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+           void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, 0, workspace,
+                   workspace_bytes, stream);
 }
 
 int fa_get_last_device_status(fa_stream_t stream) {

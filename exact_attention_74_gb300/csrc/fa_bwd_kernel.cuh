@@ -82,7 +82,8 @@ struct Params {
   __nv_bfloat16* dv;
   const float* lse2;     // [BH, nq_pad]
   const float* delta;    // [BH, nq_pad]
-  int BH, N_q, N_kv, nq_pad, causal;
+  unsigned* counters;    // [BH, n_q_tiles]: dQ partials added so far (deterministic order)
+  int BH, N_q, N_kv, nq_pad, causal, deterministic;
   int n_q_tiles, n_kv_tiles;
   float c;               // scale * log2(e)
   float scale;
@@ -95,7 +96,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
 prep_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
             const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
-            float* __restrict__ dq_acc, int BH, int N_q, int nq_pad) {
+            float* __restrict__ dq_acc, unsigned* __restrict__ counters, int BH, int N_q, int nq_pad) {
   constexpr int kPer = D / 32;     // elements per lane
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(BH) * nq_pad;
@@ -104,6 +105,7 @@ prep_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict
        r += warps) {
     const int bh = static_cast<int>(r / nq_pad);
     const int q = static_cast<int>(r % nq_pad);
+    if ((q & 127) == 0 && lane == 0) counters[r >> 7] = 0u;   // one per 128-row query tile
     if (q < N_q) {
       const size_t base = (static_cast<size_t>(bh) * N_q + q) * D + lane * kPer;
       float acc = 0.f;
@@ -176,8 +178,12 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int lane = threadIdx.x & 31;
   // Head-major order: the CTAs resident at one time cover only a few heads,
   // so their fp32 dQ accumulators (and Q, dO tiles) stay in L2.  Within a
-  // head, key tile 0 runs first: with a causal mask it sees the most query tiles.
-  const int j = static_cast<int>(blockIdx.x) % p.n_kv_tiles;
+  // head, key tile 0 runs first: with a causal mask it sees the most query
+  // tiles.  In deterministic mode each query tile takes its partials in
+  // decreasing key-tile order, so key tiles are launched from the last one:
+  // a CTA then only waits for CTAs dispatched before it.
+  const int jj = static_cast<int>(blockIdx.x) % p.n_kv_tiles;
+  const int j = p.deterministic ? p.n_kv_tiles - 1 - jj : jj;
   const int bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
   const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
   const int n_it = max(0, p.n_q_tiles - i0);
@@ -225,12 +231,24 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           // as its boxes have been read.
           if (!mbar_wait(bar(C::kStaged + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
           const int ip = i0 + t - 2;
+          unsigned* cnt = p.counters + static_cast<size_t>(bh) * p.n_q_tiles + ip;
+          if (p.deterministic) {
+            // key tiles above this one (up to the last that sees query tile ip) add first
+            const int top = p.causal ? min(ip, p.n_kv_tiles - 1) : p.n_kv_tiles - 1;
+            if (!wait_counter(cnt, static_cast<unsigned>(top - j), p.ctl, abort_flag)) break;
+            fence_proxy_async_global();
+          }
           for (int hf = 0; hf < 2; ++hf) {
             for (int c = 0; c < kBoxes; ++c)
               for (int rk = 0; rk < 4; ++rk)
                 tma_reduce_add_3d(&tmDQ, sb + C::q_off(s) + ((hf * kBoxes + c) * 4 + rk) * 4096,
                                   hf * (D / 2) + 32 * c, ip * kBN + rk * 32, bh);
             bulk_commit_group();
+          }
+          if (p.deterministic) {                 // landed: the next key tile may add
+            bulk_wait_group0();
+            fence_proxy_async_global();
+            red_release_gpu_add(cnt, 1u);
           }
         }
         if (t >= n_it) continue;
@@ -517,7 +535,7 @@ cudaError_t launch(const BwdLaunch& a) {
     const long long blocks = (rows + 7) / 8;
     prep_kernel<D><<<static_cast<unsigned>(blocks < 65535 * 8 ? blocks : 65535 * 8), 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, lse2, a.delta,
-        a.dq_acc, a.BH, a.N_q, nq_pad);
+        a.dq_acc, a.counters, a.BH, a.N_q, nq_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -527,6 +545,8 @@ cudaError_t launch(const BwdLaunch& a) {
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.lse2 = lse2;
   p.delta = a.delta;
+  p.counters = a.counters;
+  p.deterministic = a.deterministic;
   p.BH = a.BH;
   p.N_q = a.N_q;
   p.N_kv = a.N_kv;

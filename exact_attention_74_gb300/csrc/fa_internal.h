@@ -34,7 +34,9 @@ struct BwdLaunch {
   void* dk;
   void* dv;
   float* dq_acc;      // workspace: fp32 [B*H, N_q, d]
-  float* delta;       // workspace: fp32 [B*H, N_q]
+  float* delta;       // workspace: fp32 [B*H, N_q rounded up to 128], then LSE*log2e, same shape
+  unsigned* counters; // workspace: [B*H, N_q / 128 rounded up] dQ contributions applied (deterministic mode)
+  int deterministic;
   int BH, N_q, N_kv, d, causal;
   float scale;
   DevCtl ctl;

@@ -163,6 +163,41 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("barrier.cta.sync.aligned %0, %1;" :: "r"(id), "r"(count) : "memory");
 }
 
+// ------------------------------------------- cross-CTA ordering counters
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+// Order this thread's async-proxy (TMA) global accesses with its generic ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until *p == target (another CTA releases it); false after
+// flagging the status word when ctl.timeout_ns runs out.
+static __device__ __noinline__ bool wait_counter(const unsigned* p, unsigned target, const DevCtl& ctl,
+                                                 volatile int* abort) {
+  if (ld_acquire_gpu(p) == target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(p) == target) return true;
+    }
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+      atomicOr(ctl.status, kStatusTimeout);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Four fp32 atomic additions to consecutive addresses (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"

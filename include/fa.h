@@ -87,11 +87,12 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
               float tau, int emu_per_32, fa_stream_t stream);
 
 /*
- * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for this
- * problem: an fp32 dQ accumulator [B, H, N_q, d], then two fp32 row vectors
- * D = rowsum(dO * O) and LSE * log2(e), each [B, H, N_q rounded up to a
- * multiple of 128]; every part is rounded up to 256 bytes.  Returns 0 for
- * invalid sizes.
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd / fa_bwd_ex need
+ * for this problem: an fp32 dQ accumulator [B, H, N_q, d], then two fp32 row
+ * vectors D = rowsum(dO * O) and LSE * log2(e), each [B, H, N_q rounded up
+ * to a multiple of 128], then one 32-bit counter per 128-row query tile
+ * [B, H, ceil(N_q / 128)]; every part is rounded up to 256 bytes.  Returns 0
+ * for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
 
@@ -108,6 +109,27 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
            int B, int H, int N_q, int N_kv, int d, int causal, float scale,
            void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_bwd_ex -- fa_bwd with a choice of reduction order for dQ.
+ *   deterministic 0: as fa_bwd -- the partial dQ of every 128-key tile is
+ *                    added into the fp32 accumulator in whatever order the
+ *                    tiles finish (fastest; results may differ in the last
+ *                    bits from run to run).
+ *   deterministic 1: the partials of each 128-row query tile are added in a
+ *                    fixed order (decreasing key tile), so repeated calls on
+ *                    the same inputs give bit-identical dQ, dK and dV
+ *                    ("論文解説: FlashAttention-4 ...", 実験結果: the
+ *                    deterministic backward mode).  Key tiles then wait for
+ *                    one another through the workspace counters.
+ * Other arguments, the workspace and the errors are those of fa_bwd;
+ * deterministic outside {0, 1} returns FA_ERR_INVALID.
+ */
+int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O,
+              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+              int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+              int deterministic, void* workspace, size_t workspace_bytes,
+              fa_stream_t stream);
 
 /*
  * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.

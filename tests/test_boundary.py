@@ -101,10 +101,11 @@ def test_lse_needs_only_4_byte_alignment(lib):
 
 
 def test_workspace_bytes(lib):
-    # fp32 dQ accumulator + two fp32 row vectors padded to 128 rows, each rounded to 256 B
-    assert fa.fa_bwd_workspace_bytes(2, 16, 8192, 8192, 128) == 2 * 16 * 8192 * (128 * 4 + 2 * 4)
-    assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 64) == 768 + 2 * 512
-    assert fa.fa_bwd_workspace_bytes(3, 1, 130, 5, 128) == 3 * 130 * 128 * 4 + 2 * 3 * 256 * 4
+    # fp32 dQ accumulator + two fp32 row vectors padded to 128 rows + one counter per
+    # 128-row tile, each part rounded up to 256 B
+    assert fa.fa_bwd_workspace_bytes(2, 16, 8192, 8192, 128) == 2 * 16 * 8192 * (128 * 4 + 2 * 4) + 2 * 16 * 64 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 64) == 768 + 2 * 512 + 256
+    assert fa.fa_bwd_workspace_bytes(3, 1, 130, 5, 128) == 3 * 130 * 128 * 4 + 2 * 3 * 256 * 4 + 256
     assert fa.fa_bwd_workspace_bytes(1, 1, 0, 5, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 80) == 0
 
@@ -166,3 +167,15 @@ def test_valid_call_without_device_fails_loudly(lib):
     st = _fwd()
     assert st in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
     assert fa.fa_get_last_device_status(0) in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
+
+
+def test_bwd_ex_deterministic_flag(lib):
+    need = fa.fa_bwd_workspace_bytes(1, 2, 100, 90, 64)
+    for bad in (-1, 2):
+        assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, 1, 2, 100, 90, 64, 1, 0.125, bad, P, need, 0) \
+            == fa.FA_ERR_INVALID
+    # argument errors are fa_bwd's
+    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, 1, 2, 100, 90, 96, 1, 0.125, 1, P, need, 0) \
+        == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, 1, 2, 100, 90, 64, 1, 0.125, 1, P, need - 1, 0) \
+        == fa.FA_ERR_WORKSPACE

@@ -163,3 +163,60 @@ def test_full_size_backward(torch):
         q, k, v, do = (fa_inputs.bf16_bits_to_f64(x[b, h]) for x in (qb, kb, vb, dob))
         ref = oracle.head_backward(q, k, v, do, causal=w.causal, scale=w.scale)
         check_grads((dq[b, h], dk[b, h], dv[b, h]), ref, f"{w.name} b{b} h{h}")
+
+
+# ----------------------------------------------------------- deterministic mode
+
+def _bwd_ex(torch, w, t, deterministic):
+    q, k, v, o, do, lse = t
+    dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+    need = fa.fa_bwd_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)
+    st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N_q, w.N_kv, w.d,
+                      int(w.causal), w.scale, deterministic, ws.data_ptr(), need, 0)
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nkv", [(1000, 1000), (700, 300), (300, 700)])
+def test_deterministic_bitwise_repeatable_and_exact(torch, d, causal, nq, nkv):
+    w = _wl(2, 3, nq, nkv, d, causal, seed=nq + 7 * nkv + d)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, nq), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     w.B, w.H, nq, nkv, d, int(causal), w.scale, 0) == fa.FA_OK
+    t = (q, k, v, o, do, lse)
+    a = _bwd_ex(torch, w, t, 1)
+    b = _bwd_ex(torch, w, t, 1)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    ref = oracle.attention_backward(*(fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb, dob)),
+                                    causal=causal, scale=w.scale)
+    check_grads([gu.to_f64(x) for x in a], ref, f"deterministic {w.name}")
+
+
+def test_deterministic_full_size_causal(torch):
+    w = fa_inputs.WORKLOADS["bwd_8k"]
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     w.B, w.H, w.N_q, w.N_kv, w.d, 1, w.scale, 0) == fa.FA_OK
+    t = (q, k, v, o, do, lse)
+    a = _bwd_ex(torch, w, t, 1)
+    b = _bwd_ex(torch, w, t, 1)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    q64, k64, v64, do64 = (fa_inputs.bf16_bits_to_f64(x[1, 5]) for x in (qb, kb, vb, dob))
+    ref = oracle.head_backward(q64, k64, v64, do64, causal=True, scale=w.scale)
+    check_grads([gu.to_f64(x)[1, 5] for x in a], ref, "deterministic bwd_8k b1 h5")
