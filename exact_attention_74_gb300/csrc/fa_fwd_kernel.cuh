@@ -20,11 +20,12 @@
 // m_ref and P = 2^(t - m_ref); O and l are rescaled by 2^(m_ref - m_new) only
 // when the row maximum rises more than tau above m_ref.  Normalisation is
 // deferred to the epilogue (§8.1 of the first page), which also writes
-// LSE = ln2 * (m_ref + log2 l).  Two row sums are kept: l over the fp32
-// probabilities (for the LSE) and lr over the bf16-rounded probabilities that
-// the P V product actually consumes; O is divided by lr, so its weights form
-// an exact convex combination even when the largest P of a row (up to 2^tau)
-// is not a power of two.  Some of the exponentials take the FMA-pipe cubic
+// LSE = ln2 * (m_ref + log2 l), with l the sum of the fp32 probabilities.
+// O is divided by l plus the bf16 rounding residual of each block's largest
+// P (as the P V product consumes it): with tau > 0 that largest P (up to
+// 2^tau) is not a power of two, and in near-one-hot rows its rounding would
+// otherwise show in O undamped; the residuals of the other, smaller
+// probabilities average out like any bf16 rounding of P.  Some of the exponentials take the FMA-pipe cubic
 // emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
 //
 // Causal masking skips every key tile that lies wholly above the diagonal;
@@ -259,7 +260,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const float c = p.c;
     float m_ref = -INFINITY;
     float l = 0.f;      // sum of the fp32 probabilities: gives the LSE
-    float lr = 0.f;     // sum of the bf16-rounded probabilities fed to P V: normalises O
+    float lr = 0.f;     // rounding residuals of the blocks' largest P (see the header)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), j & 1, p.ctl, abort_flag));
@@ -313,7 +314,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-m_ref, -m_ref);
       float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      float sumr[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
@@ -322,12 +322,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
         sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
         const uint32_t w = pack_bf16x2(e0, e1);
-        sumr[(i & 1) * 2] = add_bf16_lo(w, sumr[(i & 1) * 2]);
-        sumr[(i & 1) * 2 + 1] = add_bf16_hi(w, sumr[(i & 1) * 2 + 1]);
         pk[i] = w;
       }
       l += (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
-      lr += (sumr[0] + sumr[1]) + (sumr[2] + sumr[3]);
+      {
+        const float pm = ex2_hw(m_blk - m_ref);                        // the block's largest P
+        const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
+        lr += pmr - pm;
+      }
       tmem_st_x64(tS, pk);
       tc_fence_before();
       mbar_arrive(bar(C::kPFull + t));
@@ -337,7 +339,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (ready) ready = mbar_wait(bar(C::kOFull + t), 0, p.ctl, abort_flag);
     if (__all_sync(0xffffffffu, ready)) {
       tc_fence_after();
-      const float inv_l = 1.f / lr;
+      const float inv_l = 1.f / (l + lr);
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {

@@ -369,20 +369,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// c + (the bf16 in the low / high half of w, widened exactly).
-__device__ __forceinline__ float add_bf16_lo(uint32_t w, float c) {
-  float d;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
-      : "=f"(d) : "r"(w), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float add_bf16_hi(uint32_t w, float c) {
-  float d;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
-      : "=f"(d) : "r"(w), "f"(c));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x (low half) = lo
   return *reinterpret_cast<uint32_t*>(&h);
