@@ -19,11 +19,14 @@
 //                        before refilling a stage it issues the TMA reduce-adds
 //                        of the dQ partial the compute warps staged there
 //              warp 1    MMA issuer, per query tile i, in this order:
-//                          dQ_i = dS K, dK += dS^T Q, dV += P^T dO,
-//                          S^T_{i+1} = K Q^T_{i+1}, dP^T_{i+1} = V dO^T_{i+1}
-//                        so that once dV is issued tile i's Q and dO are dead
-//                        and the drain of dQ_i and the P of tile i+1 overlap
-//                        the products that follow
+//                          dV += P^T dO          once P_i is in tensor memory
+//                          dQ_i = dS K, dK += dS^T Q   once dS_i is in shared memory
+//                          S^T_{i+1} = K Q^T     (overwrites P_i after dV read it)
+//                          dP^T_{i+1} = V dO^T   once dQ_i has left tensor memory
+//                        so dV overlaps the dS work, and once dK is done
+//                        tile i's Q and dO are dead and hold the drain of dQ_i
+//                        (the next tile's Q must arrive before its S, so the
+//                        S product stays after dK)
 //              warps 2-9 two warps per tensor-memory lane quarter (one key
 //                        row per thread), each warp of a pair on half of the
 //                        128 query columns: P (as soon as S is ready) back
@@ -65,7 +68,7 @@ struct Cfg {
   static constexpr int kBar = kDS + 2 * kPanel;
   // barrier indices
   static constexpr int kKVFull = 0, kQFull = 1, kStaged = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
-                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kDOFull = 11, kNumBars = 13;
+                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kDOFull = 11, kDSFull = 13, kNumBars = 14;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmem = kMisc + 16;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -198,6 +201,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kDPFull), 1);
     mbar_init(bar(C::kPFull), 256);
+    mbar_init(bar(C::kDSFull), 256);
     mbar_init(bar(C::kDQFull), 1);
     mbar_init(bar(C::kDQFree), 256);
     mbar_init(bar(C::kAccFull), 1);
@@ -310,7 +314,15 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const uint32_t sQ = sb + C::q_off(s), sdO = sb + C::do_off(s);
         const bool next = it + 1 < n_it;
         const int s1 = (it + 1) & 1;
-        ok = mbar_wait(bar(C::kPFull), it & 1, p.ctl, abort_flag);
+        ok = mbar_wait(bar(C::kPFull), it & 1, p.ctl, abort_flag);   // P_i in tensor memory
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {   // dV += P^T dO
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k, sdesc_sw128(sdO + k * 2048, kPanel, 1024), idKV,
+                 (it > 0 || k > 0) ? 1u : 0u);
+        }
+        ok = mbar_wait(bar(C::kDSFull), it & 1, p.ctl, abort_flag);  // dS_i in shared memory
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -323,15 +335,10 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
                  sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {   // dV += P^T dO
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k, sdesc_sw128(sdO + k * 2048, kPanel, 1024), idKV,
-                 (it > 0 || k > 0) ? 1u : 0u);
-        }
         // dQ_i is ready and this stage's Q and dO are no longer read: the
         // drain may stage dQ_i in them
         tc_commit(bar(C::kDQFull));
-        if (next) {                             // S of the next tile (P_i has been consumed)
+        if (next) {                             // S of the next tile (P_i was consumed by dV first)
           ok = mbar_wait(bar(C::kQFull + s1), ((it + 1) >> 1) & 1, p.ctl, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -418,6 +425,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 2, pk_keep[0]);
         tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 3, pk_keep[1]);
       }
+      tc_fence_before();
+      mbar_arrive(bar(C::kPFull));            // dV may use P now
       // ---- dS = P o (dP - D), once dP is ready
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDPFull), it & 1, p.ctl, abort_flag));
       if (!ok) break;
@@ -450,7 +459,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       }
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::kPFull));
+      mbar_arrive(bar(C::kDSFull));           // dQ and dK may read dS now
       // ---- drain this warp's half of the partial dQ (rows = queries of tile i)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), it & 1, p.ctl, abort_flag));
       if (!ok) break;
