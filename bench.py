@@ -56,6 +56,16 @@ def rank_workload(w: fa_inputs.Workload, rank: int) -> fa_inputs.Workload:
     return w.with_(seed=w.seed + 1000 * rank)
 
 
+def max_over_ranks(value: float, pg, device) -> float:
+    """The largest `value` over all ranks (a single process returns its own)."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -281,11 +291,7 @@ def run_gpu(args):
         raise fa.FAError(st, "device status after timed region")
     t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
     t_bwd = [e[1].elapsed_time(e[2]) for e in ev] if has_bwd else [0.0] * args.steps
-    ms_step = statistics.mean(a + b for a, b in zip(t_fwd, t_bwd))
-    if pg:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(statistics.mean(a + b for a, b in zip(t_fwd, t_bwd)), pg, dev)
 
     flops_step = w.fwd_flops() + (w.bwd_flops() if has_bwd else 0.0)
     value = flops_step * world / (ms_step * 1e-3) / 1e12
@@ -317,11 +323,7 @@ def run_gpu(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if pg:
-        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, dev)
 
     # ---- roofline of the dominant kernel
     peaks = measured_peaks()
