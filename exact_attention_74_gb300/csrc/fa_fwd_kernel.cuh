@@ -8,9 +8,16 @@
 //   warp 1       MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
 //                O_t += P_t V_j with P_t read from tensor memory, in the order
 //                S0 S1 | PV0 S0' PV1 S1' | ... so that the tensor core works
-//                on one tile while the softmax of the other runs.
-//   warps 2-5    softmax of tile 0, warps 6-9 softmax of tile 1; one thread
-//                owns one query row (one tensor-memory lane).
+//                on one tile while the softmax of the other runs.  The
+//                tensor core's queue is only a couple of products deep and
+//                every barrier operation of this thread is a shared-memory
+//                round trip against the operand reads, so between two groups
+//                it does one commit and the waits only, and tests the next
+//                group's barriers while it is still queueing the current one.
+//   warps 2-9    softmax of tile 0 (warps 2-5) and tile 1 (6-9); one thread
+//                owns one query row (one tensor-memory lane).  They also hand
+//                the K/V slots back to the producer: S_t,j complete implies
+//                every earlier product is complete.
 //
 // The per-row recurrence is the online softmax of "FlashAttention: GPUメモリ
 // 階層を活用したアテンション最適化の分析" §6.2 in base 2 (t = scale*log2e*s),
@@ -134,7 +141,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
-      mbar_init(bar(C::kPFull + t), 128);
+      mbar_init(bar(C::kPFull + t), 4);     // one arrive per softmax warp
       mbar_init(bar(C::kOFull + t), 1);
     }
     *abort_flag = 0;
@@ -180,7 +187,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
-      auto issue_S = [&](int t, int kslot) {
+      // S_t = Q_t K^T; after the sixth of its eight products (while the
+      // issue stalls on the tensor core's queue) run `peek`, which tests the
+      // barriers the next group waits on.
+      auto issue_S = [&](int t, int kslot, auto&& peek) {
         const uint32_t qa = sb + C::kQOff + t * C::kTileBytes;
         const uint32_t ka = sb + C::kKVOff + kslot * C::kTileBytes;
 #pragma unroll
@@ -188,6 +198,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
           mma_ss(tmem + C::col_S(t), sdesc_sw128(qa + off, 0, 1024), sdesc_sw128(ka + off, 0, 1024),
                  idS, k > 0 ? 1u : 0u);
+          if (k == D / 16 - 3) peek();
         }
       };
       auto issue_PV = [&](int t, int vslot, bool acc) {
@@ -198,53 +209,62 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                  sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, (acc || k > 0) ? 1u : 0u);
         }
       };
+      // K_j and V_j are ring loads 2j and 2j+1, in the producer's order.
+      // Their slots are released by the softmax warps (see there), so the
+      // only shared-memory operations this thread does between two groups of
+      // products are one commit and the waits.  Each of those takes a
+      // round trip through shared memory, which the tensor core keeps busy;
+      // the `peek` tests overlap them with the issue of the previous group.
+      auto kv_bar = [](int i) { return C::kKVFull + i % C::kSlots; };
+      auto kv_par = [](int i) { return static_cast<uint32_t>((i / C::kSlots) & 1); };
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
         if (n_t[t] > 0) ok = mbar_wait(bar(C::kQFull + t), 0, p.ctl, abort_flag);
-      int slot = 0;
-      uint32_t ph = 0;
-      auto next_slot = [&]() { if (++slot == C::kSlots) { slot = 0; ph ^= 1; } };
-      uint32_t pph[2] = {0, 0};
+      if (ok) ok = mbar_wait(bar(kv_bar(0)), kv_par(0), p.ctl, abort_flag);
       if (ok) {
-        const int sk = slot;
-        ok = mbar_wait(bar(C::kKVFull + sk), ph, p.ctl, abort_flag);
-        next_slot();
-        if (ok) {
-          tc_fence_after();
-          for (int t = 0; t < 2; ++t)
-            if (n_t[t] > 0) { issue_S(t, sk); tc_commit(bar(C::kSFull + t)); }
-          tc_commit(bar(C::kKVEmpty + sk));
-        }
-      }
-      for (int j = 0; j < n_max && ok; ++j) {
-        const int sv = slot;
-        ok = mbar_wait(bar(C::kKVFull + sv), ph, p.ctl, abort_flag);
-        next_slot();
-        const bool has_next = j + 1 < n_max;
-        int sk = -1;
-        if (ok && has_next) {
-          sk = slot;
-          ok = mbar_wait(bar(C::kKVFull + sk), ph, p.ctl, abort_flag);
-          next_slot();
-        }
-        if (!ok) break;
         tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) { issue_S(t, 0, [] {}); tc_commit(bar(C::kSFull + t)); }
+      }
+      uint32_t pph[2] = {0, 0};
+      bool kv_ready = false, p_ready[2] = {false, false};
+      for (int j = 0; j < n_max && ok; ++j) {
+        const int iv = 2 * j + 1, ik = 2 * j + 2;       // V_j, K_{j+1}
+        const bool has_next = j + 1 < n_max;
+        if (!kv_ready) {
+          ok = mbar_wait(bar(kv_bar(iv)), kv_par(iv), p.ctl, abort_flag);
+          if (ok && has_next) ok = mbar_wait(bar(kv_bar(ik)), kv_par(ik), p.ctl, abort_flag);
+          if (!ok) break;
+        }
+        kv_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= n_t[t]) continue;
-          ok = mbar_wait(bar(C::kPFull + t), pph[t], p.ctl, abort_flag);
+          if (!p_ready[t]) ok = mbar_wait(bar(C::kPFull + t), pph[t], p.ctl, abort_flag);
           pph[t] ^= 1;
+          p_ready[t] = false;
           if (!ok) break;
           tc_fence_after();
-          issue_PV(t, sv, j > 0);
+          issue_PV(t, iv % C::kSlots, j > 0);
           if (j + 1 < n_t[t]) {
-            issue_S(t, sk);
+            if (t == 0) {
+              issue_S(0, ik % C::kSlots, [&] {
+                if (j < n_t[1]) p_ready[1] = mbar_test_wait(bar(C::kPFull + 1), pph[1]);
+              });
+            } else {
+              issue_S(1, ik % C::kSlots, [&] {
+                const int iv2 = iv + 2, ik2 = ik + 2;   // V_{j+1}, K_{j+2}
+                const bool a = mbar_test_wait(bar(kv_bar(iv2)), kv_par(iv2));
+                const bool b = ik2 >= 2 * n_max || mbar_test_wait(bar(kv_bar(ik2)), kv_par(ik2));
+                const bool c = j + 1 >= n_t[0] || mbar_test_wait(bar(C::kPFull + 0), pph[0]);
+                kv_ready = a && b;
+                p_ready[0] = c && j + 1 < n_t[0];
+              });
+            }
             tc_commit(bar(C::kSFull + t));
           } else {
             tc_commit(bar(C::kOFull + t));
           }
         }
-        tc_commit(bar(C::kKVEmpty + sv));
-        if (has_next) tc_commit(bar(C::kKVEmpty + sk));
       }
     }
   } else {
@@ -257,6 +277,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::col_S(t);
     const uint32_t tO = tmem + lane_addr + C::col_O(t);
+    const bool releaser = t == (n_t[1] > 0 ? 1 : 0);
     const float c = p.c;
     float m_ref = -INFINITY;
     float l = 0.f;      // sum of the fp32 probabilities: gives the LSE
@@ -265,6 +286,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     for (int j = 0; j < nt; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), j & 1, p.ctl, abort_flag));
       if (!ok) break;
+      // S_t,j complete means every product queued before it is complete too:
+      // the tile that runs to the last key tile (tile 1 unless it is empty)
+      // hands K_j and V_{j-1} back to the producer.
+      if (releaser && r_in_tile == 0) {
+        mbar_arrive(bar(C::kKVEmpty + (2 * j) % C::kSlots));
+        if (j > 0) mbar_arrive(bar(C::kKVEmpty + (2 * j - 1) % C::kSlots));
+      }
       tc_fence_after();
       uint32_t s[128];
       tmem_ld_x128(tS, s);
@@ -330,9 +358,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
         lr += pmr - pm;
       }
-      tmem_st_x64(tS, pk);
+      tmem_st_x64(tS, pk);   // waits for its own stores
       tc_fence_before();
-      mbar_arrive(bar(C::kPFull + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kPFull + t));
     }
     // ------------------------------------------------------------- epilogue
     bool ready = ok && nt > 0;
