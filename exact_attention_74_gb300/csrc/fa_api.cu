@@ -42,6 +42,7 @@ struct DevState {
   bool checked = false;
   bool supported = false;
   unsigned* status = nullptr;
+  int n_sms = 0;
 };
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
@@ -58,8 +59,9 @@ int check_sizes(int B, int H, int N_q, int N_kv, int d, int causal, float scale)
 }  // namespace
 
 // Resolve the current device: must be compute capability 10.3 (sm_103a code
-// only); returns the watchdog handle for its kernels.
-int device_ctl(DevCtl* ctl) {
+// only); returns the watchdog handle for its kernels and, if asked, its
+// multiprocessor count.
+int device_ctl(DevCtl* ctl, int* n_sms) {
   static std::mutex mu;
   static DevState states[128];
   int dev = -1;
@@ -78,6 +80,10 @@ int device_ctl(DevCtl* ctl) {
       return FA_ERR_CUDA;
     }
     s.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&s.n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
     if (s.supported) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
@@ -91,6 +97,7 @@ int device_ctl(DevCtl* ctl) {
   if (!s.supported) return FA_ERR_UNSUPPORTED;
   ctl->status = s.status;
   ctl->timeout_ns = g_timeout_ns.load();
+  if (n_sms) *n_sms = s.n_sms;
   return FA_OK;
 }
 
@@ -203,7 +210,7 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const 
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (misaligned(workspace, 256)) return FA_ERR_ALIGN;
   BwdLaunch a;
-  st = device_ctl(&a.ctl);
+  st = device_ctl(&a.ctl, &a.n_sms);
   if (st != FA_OK) return st;
   const int BH = B * H;
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;

@@ -88,6 +88,7 @@ struct Params {
   unsigned* counters;    // [BH, n_q_tiles]: dQ partials added so far (deterministic order)
   int BH, N_q, N_kv, nq_pad, causal, deterministic;
   int n_q_tiles, n_kv_tiles;
+  int n_sms;             // CTAs resident at once (one per SM)
   float c;               // scale * log2(e)
   float scale;
   DevCtl ctl;
@@ -253,6 +254,20 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             bulk_wait_group0();
             fence_proxy_async_global();
             red_release_gpu_add(cnt, 1u);
+          }
+        }
+        if (t == max(0, n_it - 4)) {
+          // The CTA that this SM (or another) runs one wave later reads a
+          // K/V tile nobody has touched yet: start it towards L2 now.
+          const int nb = static_cast<int>(blockIdx.x) + p.n_sms;
+          if (nb < static_cast<int>(gridDim.x)) {
+            const int njj = nb % p.n_kv_tiles;
+            const int nj = p.deterministic ? p.n_kv_tiles - 1 - njj : njj;
+            const int nbh = nb / p.n_kv_tiles;
+            for (int pn = 0; pn < D / 64; ++pn) {
+              tma_prefetch_l2_3d(&tmK, pn * 64, nj * kBM, nbh);
+              tma_prefetch_l2_3d(&tmV, pn * 64, nj * kBM, nbh);
+            }
           }
         }
         if (t >= n_it) continue;
@@ -494,32 +509,44 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     ready = __all_sync(0xffffffffu, ready);
     if (n_it == 0 || ready) {
       if (n_it > 0) tc_fence_after();
-      const size_t rowoff = (static_cast<size_t>(bh) * p.N_kv + kg) * D + half * (D / 2);
+      // Each warp owns 32 key rows x D/2 columns of dV and of dK.  Its rows
+      // go through its own slice of the (now unused) dS buffer, so that the
+      // global stores cover whole 128-byte lines instead of one 16-byte
+      // piece of 32 different rows.
+      constexpr int kCpr = D / 16;                // 16-byte chunks per row slice
+      constexpr int kRowsPerStore = 32 / kCpr;
+      uint8_t* slice = smem + C::kDS + (warp - 2) * (32 * D);   // 32 rows x D/2 bf16
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* outp = (which == 0 ? p.dv : p.dk) + rowoff;
         const float f = which == 0 ? 1.f : p.scale;
-        const uint32_t col = (which == 0 ? C::kColDV : C::kColDK) + half * (D / 2);
-#pragma unroll 1
-        for (int ch = 0; ch < D / 64; ++ch) {
-          uint32_t v[32];
-          if (n_it > 0) {
-            tmem_ld_x32(tmem + lane_addr + col + 32 * ch, v);
-          } else {
+        uint32_t v[D / 2];
+        if (n_it > 0) {
+          const uint32_t col = (which == 0 ? C::kColDV : C::kColDK) + half * (D / 2);
+          if constexpr (D == 128) tmem_ld_x64(tmem + lane_addr + col, v);
+          else tmem_ld_x32(tmem + lane_addr + col, v);
+        } else {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) v[u] = 0u;
-          }
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(outp + 32 * ch);
+          for (int u = 0; u < D / 2; ++u) v[u] = 0u;
+        }
+        __syncwarp();                             // the previous output's reads are done
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t w4[4];
+        for (int c = 0; c < kCpr; ++c) {
+          uint32_t w4[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w4[e] = pack_bf16x2(__uint_as_float(v[8 * u + 2 * e]) * f, __uint_as_float(v[8 * u + 2 * e + 1]) * f);
-              dst[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          }
+          for (int e = 0; e < 4; ++e)
+            w4[e] = pack_bf16x2(__uint_as_float(v[8 * c + 2 * e]) * f, __uint_as_float(v[8 * c + 2 * e + 1]) * f);
+          *reinterpret_cast<uint4*>(slice + lane * (D / 2 * 2) + ((c ^ (lane % kCpr)) * 16)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        __syncwarp();
+        __nv_bfloat16* outp = (which == 0 ? p.dv : p.dk) + static_cast<size_t>(bh) * p.N_kv * D + half * (D / 2);
+#pragma unroll
+        for (int k = 0; k < kCpr; ++k) {
+          const int rr = k * kRowsPerStore + lane / kCpr;    // row within the warp's 32
+          const int cc = lane % kCpr;
+          const int key = j * kBM + rank * 32 + rr;
+          const uint4 w = *reinterpret_cast<const uint4*>(slice + rr * (D / 2 * 2) + ((cc ^ (rr % kCpr)) * 16));
+          if (key < p.N_kv) *reinterpret_cast<uint4*>(outp + static_cast<size_t>(key) * D + cc * 8) = w;
         }
       }
     }
@@ -566,6 +593,7 @@ cudaError_t launch(const BwdLaunch& a) {
   p.c = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.scale = a.scale;
   p.ctl = a.ctl;
+  p.n_sms = a.n_sms;
   auto kern = main_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;

@@ -38,6 +38,7 @@ struct BwdLaunch {
   unsigned* counters; // workspace: [B*H, N_q / 128 rounded up] dQ contributions applied (deterministic mode)
   int deterministic;
   int BH, N_q, N_kv, d, causal;
+  int n_sms;          // multiprocessor count of the device
   float scale;
   DevCtl ctl;
   cudaStream_t stream;
@@ -46,7 +47,7 @@ struct BwdLaunch {
 cudaError_t launch_bwd(const BwdLaunch& a);
 
 // Defined in fa_api.cu.
-int device_ctl(DevCtl* ctl);
+int device_ctl(DevCtl* ctl, int* n_sms = nullptr);
 int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows = 128);
 int make_map_f32(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_cols, int box_rows);
 
