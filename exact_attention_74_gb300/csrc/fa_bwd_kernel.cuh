@@ -399,41 +399,42 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       // ---- P = 2^(S c - LSE log2 e), as soon as S is ready
       float pf[2][32];
       uint32_t pk_keep[2][16];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int ch = 2 * half + cc;        // 32-query chunk
-        uint32_t sv[32];
-        tmem_ld_x32(tmem + lane_addr + C::kColS + 32 * ch, sv);
+      {
+        // both 32-query chunks of this warp in one tensor-memory round trip
+        uint32_t sv[64];
+        tmem_ld_x64(tmem + lane_addr + C::kColS + 64 * half, sv);
         // P of chunk ch lands on the S columns of queries [16 ch, 16 ch + 16),
-        // which the first warp of the pair reads in its second chunk: it
-        // signals once those reads are done, the second warp writes after.
-        if (half == 0 && cc == 1) named_bar_arrive(pair_bar, 64);
-        uint32_t pk[16];
+        // which the first warp of the pair has now read: the second warp
+        // writes after this signal.
+        if (half == 0) named_bar_arrive(pair_bar, 64);
 #pragma unroll
-        for (int u = 0; u < 32; u += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * ch + u);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int ch = 2 * half + cc;        // 32-query chunk
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int q = u + 2 * h;
-            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-            const float2 x = fma2(make_float2(__uint_as_float(sv[q]), __uint_as_float(sv[q + 1])), c2, nl);
-            pf[cc][q] = ex2_hw(x.x);
-            pf[cc][q + 1] = ex2_hw(x.y);
+          for (int u = 0; u < 32; u += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * ch + u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int q = u + 2 * h;
+              const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+              const float2 x = fma2(make_float2(__uint_as_float(sv[32 * cc + q]), __uint_as_float(sv[32 * cc + q + 1])),
+                                    c2, nl);
+              pf[cc][q] = ex2_hw(x.x);
+              pf[cc][q + 1] = ex2_hw(x.y);
+            }
           }
-        }
-        if (masked) {
+          if (masked) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (!key_ok || 32 * ch + q < lim) pf[cc][q] = 0.f;
-        }
+            for (int q = 0; q < 32; ++q)
+              if (!key_ok || 32 * ch + q < lim) pf[cc][q] = 0.f;
+          }
 #pragma unroll
-        for (int q = 0; q < 32; q += 2) pk[q >> 1] = pack_bf16x2(pf[cc][q], pf[cc][q + 1]);
-        if (half == 0) {
-          tmem_st_x16(tmem + lane_addr + C::kColS + 16 * ch, pk);
-        } else {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) pk_keep[cc][u] = pk[u];
+          for (int q = 0; q < 32; q += 2) pk_keep[cc][q >> 1] = pack_bf16x2(pf[cc][q], pf[cc][q + 1]);
         }
+      }
+      if (half == 0) {
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 0, pk_keep[0]);
+        tmem_st_x16(tmem + lane_addr + C::kColS + 16 * 1, pk_keep[1]);
       }
       if (half == 1) {
         named_bar_sync(pair_bar, 64);
@@ -446,11 +447,13 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDPFull), it & 1, p.ctl, abort_flag));
       if (!ok) break;
       tc_fence_after();
+      uint32_t dpv[64];
+      tmem_ld_x64(tmem + lane_addr + C::kColDP + 64 * half, dpv);   // both chunks at once
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int ch = 2 * half + cc;
-        uint32_t dp[32], dk[16];
-        tmem_ld_x32(tmem + lane_addr + C::kColDP + 32 * ch, dp);
+        uint32_t dk[16];
+        const uint32_t* dp = dpv + 32 * cc;
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(dlt_s + 32 * ch + u);
@@ -481,9 +484,17 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       tc_fence_after();
       constexpr int kBoxes = D / 64;          // 32-column boxes per warp
       uint32_t v[kBoxes][32];
+      if constexpr (kBoxes == 2) {
+        uint32_t vv[64];
+        tmem_ld_x64(tmem + lane_addr + C::kColDP + half * (D / 2), vv);
 #pragma unroll
-      for (int c = 0; c < kBoxes; ++c)
-        tmem_ld_x32(tmem + lane_addr + C::kColDP + half * (D / 2) + 32 * c, v[c]);
+        for (int u = 0; u < 32; ++u) {
+          v[0][u] = vv[u];
+          v[1][u] = vv[32 + u];
+        }
+      } else {
+        tmem_ld_x32(tmem + lane_addr + C::kColDP + half * (D / 2), v[0]);
+      }
       tc_fence_before();
       mbar_arrive_relaxed(bar(C::kDQFree));   // the tensor-memory reads are complete
       // Stage each 32-row x 32-column fp32 box in tile i's dead Q/dO buffers,
