@@ -20,7 +20,8 @@
 //                        of the dQ partial the compute warps staged there
 //              warp 1    MMA issuer, per query tile i, in this order:
 //                          dV += P^T dO          once P_i is in tensor memory
-//                          dQ_i = dS K, dK += dS^T Q   once dS_i is in shared memory
+//                          dQ_i = dS K           once dS_i is in shared memory
+//                          dK += dS^T Q          once dS^T_i is in tensor memory
 //                          S^T_{i+1} = K Q^T     (overwrites P_i after dV read it)
 //                          dP^T_{i+1} = V dO^T   once dQ_i has left tensor memory
 //                        so dV overlaps the dS work, and once dK is done
@@ -39,8 +40,9 @@
 //            dK and dV stay in tensor memory for the whole loop and are
 //            written once at the end.
 //   convert -- dQ = bf16(scale * accumulator).
-// Tensor-memory columns: S^T/P^T [0,128), dP^T and then the partial dQ
-// [128,256), dV [256,256+D), dK [256+D,256+2D).
+// Tensor-memory columns: S^T [0,128), over which P^T [0,64) and dS^T
+// [64,128) land as bf16 pairs (the A operands of dV and dK); dP^T and then
+// the partial dQ [128,256); dV [256,256+D); dK [256+D,256+2D).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -68,10 +70,11 @@ struct Cfg {
   static constexpr int kBar = kDS + 2 * kPanel;
   // barrier indices
   static constexpr int kKVFull = 0, kQFull = 1, kStaged = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
-                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kDOFull = 11, kDSFull = 13, kNumBars = 14;
+                       kDQFree = 8, kAccFull = 9, kDPFull = 10, kDOFull = 11, kDSFull = 13, kDSTFull = 14,
+                       kNumBars = 15;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmem = kMisc + 16;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr uint32_t kColS = 0, kColDS = 64, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
   static __device__ constexpr int q_off(int s) { return kStage0 + s * kStageBytes; }
   static __device__ constexpr int do_off(int s) { return kStage0 + s * kStageBytes + kTile; }
@@ -203,6 +206,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(bar(C::kDPFull), 1);
     mbar_init(bar(C::kPFull), 256);
     mbar_init(bar(C::kDSFull), 256);
+    mbar_init(bar(C::kDSTFull), 256);
     mbar_init(bar(C::kDQFull), 1);
     mbar_init(bar(C::kDQFree), 256);
     mbar_init(bar(C::kAccFull), 1);
@@ -345,10 +349,13 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + k * 2048, kPanel, 1024),
                  sdesc_sw128(sK + k * 2048, kPanel, 1024), idQ, k > 0);
         }
+        ok = mbar_wait(bar(C::kDSTFull), it & 1, p.ctl, abort_flag); // dS^T_i in tensor memory
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {   // dK += dS^T Q  (unscaled)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (k >> 2) * kPanel + (k & 3) * 32, 0, 1024),
-                 sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kBN / 16; ++k) {   // dK += dS^T Q  (unscaled; dS^T from tensor memory)
+          mma_ts(tmem + C::kColDK, tmem + C::kColDS + 8 * k, sdesc_sw128(sQ + k * 2048, kPanel, 1024), idKV,
+                 (it > 0 || k > 0) ? 1u : 0u);
         }
         // dQ_i is ready and this stage's Q and dO are no longer read: the
         // drain may stage dQ_i in them
@@ -380,7 +387,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
     const bool key_ok = kg < p.N_kv;
     const float2 c2 = make_float2(p.c, p.c);
-    const uint32_t pair_bar = 1 + rank;      // named barrier of the two warps of this lane quarter
+    const uint32_t pair_bar = 1 + rank;      // named barriers of the two warps of this lane quarter:
+    const uint32_t pair_bar2 = 5 + rank;     // first -> second warp (S read), second -> first
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
@@ -388,7 +396,10 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       bool w = mbar_wait(bar(C::kSFull), it & 1, p.ctl, abort_flag);
       if (w) w = mbar_wait(bar(C::kQFull + s), (it >> 1) & 1, p.ctl, abort_flag);
       ok = __all_sync(0xffffffffu, w);
-      if (!ok) break;
+      if (!ok) {
+        named_bar_arrive(half == 0 ? pair_bar : pair_bar2, 64);   // the other warp may wait on it
+        break;
+      }
       tc_fence_after();
       const float* lse_s = reinterpret_cast<const float*>(smem + C::lse_off(s));
       const float* dlt_s = reinterpret_cast<const float*>(smem + C::dlt_off(s));
@@ -406,7 +417,9 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         // P of chunk ch lands on the S columns of queries [16 ch, 16 ch + 16),
         // which the first warp of the pair has now read: the second warp
         // writes after this signal.
-        if (half == 0) named_bar_arrive(pair_bar, 64);
+        // The second warp's dS^T later lands on the S columns [64, 96) that
+        // the second warp reads: it signals once it has read them.
+        named_bar_arrive(half == 0 ? pair_bar : pair_bar2, 64);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int ch = 2 * half + cc;        // 32-query chunk
@@ -450,9 +463,11 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       uint32_t dpv[64];
       tmem_ld_x64(tmem + lane_addr + C::kColDP + 64 * half, dpv);   // both chunks at once
 #pragma unroll
+      uint32_t dsk[2][16];
+#pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int ch = 2 * half + cc;
-        uint32_t dk[16];
+        uint32_t (&dk)[16] = dsk[cc];
         const uint32_t* dp = dpv + 32 * cc;
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
@@ -476,8 +491,16 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
       }
       fence_async_smem();
+      mbar_arrive(bar(C::kDSFull));           // dQ may read dS now
+      // dS^T (bf16 pairs) also into tensor memory over the dead S columns
+      // [64, 128), where dK reads it (queued after dQ, so this is off the
+      // critical path): the first warp's half overwrites S columns the
+      // second warp read, so it waits for that warp's signal.
+      if (half == 0) named_bar_sync(pair_bar2, 64);
+      tmem_st_x16(tmem + lane_addr + C::kColDS + 32 * half, dsk[0]);
+      tmem_st_x16(tmem + lane_addr + C::kColDS + 32 * half + 16, dsk[1]);
       tc_fence_before();
-      mbar_arrive(bar(C::kDSFull));           // dQ and dK may read dS now
+      mbar_arrive(bar(C::kDSTFull));          // dK may read dS^T now
       // ---- drain this warp's half of the partial dQ (rows = queries of tile i)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), it & 1, p.ctl, abort_flag));
       if (!ok) break;
