@@ -462,7 +462,6 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       tc_fence_after();
       uint32_t dpv[64];
       tmem_ld_x64(tmem + lane_addr + C::kColDP + 64 * half, dpv);   // both chunks at once
-#pragma unroll
       uint32_t dsk[2][16];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
