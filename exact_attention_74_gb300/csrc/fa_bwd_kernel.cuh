@@ -71,7 +71,7 @@ struct Cfg {
   // barrier indices
   static constexpr int kKVFull = 0, kQFull = 1, kStaged = 3, kSFull = 5, kPFull = 6, kDQFull = 7,
                        kDQFree = 8, kAccFull = 9, kDPFull = 10, kDOFull = 11, kDSFull = 13, kDSTFull = 14,
-                       kNumBars = 15;
+                       kStagedQ = 15, kNumBars = 17;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmem = kMisc + 16;
   static constexpr uint32_t kColS = 0, kColDS = 64, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -201,6 +201,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       mbar_init(bar(C::kQFull + s), 1);      // Q tile + LSE and D rows
       mbar_init(bar(C::kDOFull + s), 1);     // dO tile
       mbar_init(bar(C::kStaged + s), 8);       // one arrive per compute warp once its dQ boxes are staged
+      mbar_init(bar(C::kStagedQ + s), 8);      // ... once its boxes in the Q buffer are
     }
     mbar_init(bar(C::kSFull), 1);
     mbar_init(bar(C::kDPFull), 1);
@@ -236,9 +237,10 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         if (t >= 2) {
           // Tile t-2 staged its partial dQ in stage s (its Q and dO were no
           // longer read): add it into the accumulator in two groups, the
-          // boxes held in the Q buffer first, and refill each buffer as soon
-          // as its boxes have been read.
-          if (!mbar_wait(bar(C::kStaged + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
+          // boxes held in the Q buffer first (the compute warps stage those
+          // first and signal them on their own: the next Q waits on them),
+          // and refill each buffer as soon as its boxes have been read.
+          if (!mbar_wait(bar(C::kStagedQ + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
           const int ip = i0 + t - 2;
           unsigned* cnt = p.counters + static_cast<size_t>(bh) * p.n_q_tiles + ip;
           if (p.deterministic) {
@@ -247,13 +249,18 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             if (!wait_counter(cnt, static_cast<unsigned>(top - j), p.ctl, abort_flag)) break;
             fence_proxy_async_global();
           }
-          for (int hf = 0; hf < 2; ++hf) {
-            for (int c = 0; c < kBoxes; ++c)
-              for (int rk = 0; rk < 4; ++rk)
-                tma_reduce_add_3d(&tmDQ, sb + C::q_off(s) + ((hf * kBoxes + c) * 4 + rk) * 4096,
-                                  hf * (D / 2) + 32 * c, ip * kBN + rk * 32, bh);
+          // box (hf, c, rk): columns hf * D/2 + 32 c, rows 32 rk of the tile,
+          // at q_off + c * kTile + (4 hf + rk) * 4 KB; group c
+          for (int c = 0; c < 2; ++c) {
+            if (c == 1 && !mbar_wait(bar(C::kStaged + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
+            if (c < kBoxes)
+              for (int hf = 0; hf < 2; ++hf)
+                for (int rk = 0; rk < 4; ++rk)
+                  tma_reduce_add_3d(&tmDQ, sb + C::q_off(s) + c * C::kTile + (hf * 4 + rk) * 4096,
+                                    hf * (D / 2) + 32 * c, ip * kBN + rk * 32, bh);
             bulk_commit_group();
           }
+          if (*abort_flag) break;
           if (p.deterministic) {                 // landed: the next key tile may add
             bulk_wait_group0();
             fence_proxy_async_global();
@@ -522,19 +529,28 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       // Stage each 32-row x 32-column fp32 box in tile i's dead Q/dO buffers,
       // laid out as TMA's 128-byte swizzle expects (row = lane, 16-byte chunk
       // j at j ^ (row & 7)); the producer adds the boxes into the accumulator.
+      // Box c of this warp (columns half * D/2 + 32 c, rows 32 rank) goes to
+      // q_off + c * kTile + (4 half + rank) * 4 KB: with d = 128 box 0 is in
+      // the Q buffer and box 1 in the dO buffer, and the Q buffer's boxes are
+      // signalled first, since the next Q tile waits for them to be read.
       const uint32_t stage = sb + C::q_off(s);
 #pragma unroll
       for (int c = 0; c < kBoxes; ++c) {
-        const uint32_t box = stage + ((half * kBoxes + c) * 4 + rank) * 4096;
+        const uint32_t box = stage + c * C::kTile + (half * 4 + rank) * 4096;
         uint8_t* rowp = smem + (box - sb) + lane * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(rowp + ((u ^ (lane & 7)) * 16)) =
               make_uint4(v[c][4 * u], v[c][4 * u + 1], v[c][4 * u + 2], v[c][4 * u + 3]);
+        if (c == 0) {
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::kStagedQ + s));
+        }
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kStaged + s));   // the producer reduces it
+      if (lane == 0) mbar_arrive(bar(C::kStaged + s));   // the producer reduces the rest
     }
     // ----------------------------------------------------- dK, dV epilogue
     bool ready = ok;
