@@ -51,7 +51,7 @@ int check_sizes(int B, int H, int N_q, int N_kv, int d, int causal, float scale)
   if (B < 1 || H < 1 || N_q < 1 || N_kv < 1) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID;
   return FA_OK;
 }
@@ -158,9 +158,10 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
   st = device_ctl(&a.ctl);
   if (st != FA_OK) return st;
   const int BH = B * H;
+  const int kv_rows = d == 256 ? 64 : 128;   // rows per K/V box (the d = 256 kernel steps 64 keys)
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
-  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH)) != FA_OK) return st;
-  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH, kv_rows)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH, kv_rows)) != FA_OK) return st;
   a.o = O;
   a.lse = LSE;
   a.BH = BH;
@@ -172,7 +173,7 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
   a.tau = tau;
   a.emu_per_32 = emu_per_32;
   a.stream = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = (d == 64) ? launch_fwd_d64(a) : launch_fwd_d128(a);
+  const cudaError_t e = (d == 64) ? launch_fwd_d64(a) : (d == 128) ? launch_fwd_d128(a) : launch_fwd_d256(a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -186,7 +187,7 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
-  if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK) return 0;
+  if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK || d == 256) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N_q;
   const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(N_q) + 127) / 128 * 128);
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
@@ -201,6 +202,7 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const 
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID;
   int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
   if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;   // the backward kernel covers d = 64 and 128
   if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID;
   if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
       misaligned(dO, 16) || misaligned(dQ, 16) || misaligned(dK, 16) || misaligned(dV, 16) ||

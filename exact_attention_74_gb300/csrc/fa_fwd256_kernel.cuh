@@ -1,0 +1,390 @@
+// fa_fwd256_kernel.cuh -- forward exact attention for head dimension 256.
+//
+// At d = 256 one query tile's O already takes half of tensor memory (256
+// fp32 columns), so the two-tile ping-pong of the d <= 128 kernel does not
+// fit.  Instead one CTA owns one 128-row query tile and overlaps the work of
+// consecutive key steps of that tile (64 keys per step):
+//
+//   tensor memory   S_j in one of two 64-column buffers [0,64) / [64,128),
+//                   Q as bf16 pairs [128,256) (copied in once), O [256,512)
+//   warp 0          TMA producer: Q once (64 KB), then K_j, V_j (32 KB each)
+//                   into a ring of five shared-memory slots
+//   warp 1          MMA issuer (one thread): S_{j+1} = Q K_{j+1}^T (A from
+//                   tensor memory, so only K is read from shared memory) is
+//                   queued before O += P_j V_j, so the tensor core computes
+//                   the next scores while the softmax of the current ones runs
+//   warps 2-5       softmax, one thread per query row (one tensor-memory lane)
+//
+// The per-row recurrence is the same online softmax in base 2 with the
+// conditional rescaling of "論文解説: FlashAttention-4 — Algorithm and Kernel
+// Pipelining Co-Design for Asymmetric Hardware Scaling" (条件付きオンライン
+// softmaxリスケーリング) as the d <= 128 kernel, including the deferred
+// normalisation by l plus each block's max-element rounding residual.  The
+// rare O rescale must not race with the previous step's P V (queued after
+// S_j), so it first waits for that product's completion, which the release
+// of V_{j-1}'s ring slot signals.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "exp2.cuh"
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace fwd256 {
+
+constexpr int D = 256;
+constexpr int kBM = 128;                  // query rows per CTA
+constexpr int kBN = 64;                   // keys per step
+constexpr int kThreads = 192;             // 6 warps
+constexpr int kSlots = 5;                 // K/V ring
+constexpr int kQPanel = 128 * 128;        // 128 rows x 128 B (64 bf16) swizzle panel
+constexpr int kKPanel = 64 * 128;         // 64 rows x 128 B
+constexpr int kQBytes = 4 * kQPanel;      // 64 KB
+constexpr int kSlotBytes = 4 * kKPanel;   // 32 KB
+constexpr int kQOff = 0;
+constexpr int kKVOff = kQBytes;
+constexpr int kBarOff = kKVOff + kSlots * kSlotBytes;
+// barrier indices
+constexpr int kQFull = 0;                 // Q tile in shared memory
+constexpr int kQReady = 1;                // Q in tensor memory
+constexpr int kKVFull = 2;                // kSlots
+constexpr int kKVEmpty = 2 + kSlots;      // kSlots
+constexpr int kSFull = 2 + 2 * kSlots;    // 2 (per S buffer)
+constexpr int kPFull = 4 + 2 * kSlots;    // 2 (per S buffer)
+constexpr int kOFull = 6 + 2 * kSlots;
+constexpr int kNumBars = 7 + 2 * kSlots;
+constexpr int kMiscOff = kBarOff + 8 * kNumBars;   // tmem base, abort flag
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + base alignment slack
+// tensor-memory columns
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColQ = 128;
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 512;
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  int BH, N_q, N_kv, causal;
+  int n_qtiles;   // ceil(N_q / 128)
+  int n_steps;    // ceil(N_kv / 64)
+  float c;        // scale * log2(e)
+  float tau;      // log2 units
+  DevCtl ctl;
+};
+
+// K/V ring: load i is K_{i/2} (even i) or V_{i/2} (odd i).
+__device__ __forceinline__ int ring_slot(int i) { return i % kSlots; }
+__device__ __forceinline__ uint32_t ring_phase(int i) { return static_cast<uint32_t>((i / kSlots) & 1); }
+
+template <int EMU>
+__device__ __forceinline__ float ex2_mix(float x, int col) {
+  if ((col & 31) < EMU) return ex2_poly3(x);
+  return ex2_hw(x);
+}
+
+template <int EMU>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + kBarOff + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work tile: one query tile of one (batch, head); causal grids run the
+  // heaviest tiles (the last query rows) first.
+  int qt, bh;
+  if (p.causal) {
+    qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else {
+    qt = static_cast<int>(blockIdx.x) % p.n_qtiles;
+    bh = static_cast<int>(blockIdx.x) / p.n_qtiles;
+  }
+  const int qbase = qt * kBM;
+  // key steps this tile sees (causal: keys up to its last row, qbase + 127)
+  const int n = p.causal ? min(p.n_steps, (qbase + kBM) / kBN) : p.n_steps;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQReady), 4);             // one arrive per softmax warp
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(kKVFull + s), 1);
+      mbar_init(bar(kKVEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kSFull + b), 1);
+      mbar_init(bar(kPFull + b), 4);        // one arrive per softmax warp
+    }
+    mbar_init(bar(kOFull), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      mbar_arrive_expect_tx(bar(kQFull), kQBytes);
+      for (int pn = 0; pn < 4; ++pn)
+        tma_load_3d(sb + kQOff + pn * kQPanel, &tmQ, bar(kQFull), pn * 64, qbase, bh);
+      const uint64_t keep = l2_policy_evict_last();
+      for (int i = 0; i < 2 * n; ++i) {
+        const int s = ring_slot(i);
+        if (!mbar_wait(bar(kKVEmpty + s), ring_phase(i) ^ 1, p.ctl, abort_flag)) break;
+        const uint32_t dst = sb + kKVOff + s * kSlotBytes;
+        mbar_arrive_expect_tx(bar(kKVFull + s), kSlotBytes);
+        for (int pn = 0; pn < 4; ++pn)
+          tma_load_3d_hint(dst + pn * kKPanel, (i & 1) ? &tmV : &tmK, bar(kKVFull + s), pn * 64,
+                           (i >> 1) * kBN, bh, keep);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+      auto slot_addr = [&](int i) { return sb + kKVOff + ring_slot(i) * kSlotBytes; };
+      auto kv_wait = [&](int i) { return mbar_wait(bar(kKVFull + ring_slot(i)), ring_phase(i), p.ctl, abort_flag); };
+      auto issue_S = [&](int j) {          // S_j = Q K_j^T into S buffer j & 1
+        const uint32_t ka = slot_addr(2 * j);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ts(tmem + kColS + 64 * (j & 1), tmem + kColQ + 8 * k,
+                 sdesc_sw128(ka + (k >> 2) * kKPanel + (k & 3) * 32, 0, 1024), idS, k > 0 ? 1u : 0u);
+      };
+      auto issue_PV = [&](int j) {         // O += P_j V_j, P_j over S buffer j & 1
+        const uint32_t va = slot_addr(2 * j + 1);
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          mma_ts(tmem + kColO, tmem + kColS + 64 * (j & 1) + 8 * k, sdesc_sw128(va + k * 2048, kKPanel, 1024),
+                 idO, (j > 0 || k > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(kQReady), 0, p.ctl, abort_flag);
+      if (ok) ok = kv_wait(0);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+        tc_commit(bar(kSFull + 0));
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        if (j + 1 < n) {
+          // the next scores first; their buffer held P_{j-1}, which the P V
+          // queued in the previous step has read
+          if (!(ok = kv_wait(2 * j + 2))) break;
+          tc_fence_after();
+          issue_S(j + 1);
+          tc_commit(bar(kSFull + ((j + 1) & 1)));
+        }
+        tc_commit(bar(kKVEmpty + ring_slot(2 * j)));          // K_j: read by S_j, queued before
+        if (!(ok = kv_wait(2 * j + 1))) break;
+        if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
+        tc_fence_after();
+        issue_PV(j);
+        tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));      // V_j (and: P V_j is complete)
+      }
+      if (ok) tc_commit(bar(kOFull));
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int rank = warp & 3;              // tensor-memory lane quarter
+    const int r_in_tile = rank * 32 + lane;
+    const int row = qbase + r_in_tile;
+    const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
+    const uint32_t tO = tmem + lane_addr + kColO;
+    const float c = p.c;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kQFull), 0, p.ctl, abort_flag));
+    if (ok) {
+      // Q row into tensor memory as bf16 pairs (column w holds d = 2w, 2w+1),
+      // read from TMA's 128-byte swizzled panels (chunk c at c ^ (row & 7)).
+      uint32_t qa[64], qb[64];
+#pragma unroll
+      for (int pn = 0; pn < 4; ++pn) {
+        const uint8_t* rp = smem + kQOff + pn * kQPanel + r_in_tile * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + ((ch ^ (r_in_tile & 7)) * 16));
+          uint32_t* dst = (pn < 2 ? qa : qb) + (pn & 1) * 32 + ch * 4;
+          dst[0] = w.x;
+          dst[1] = w.y;
+          dst[2] = w.z;
+          dst[3] = w.w;
+        }
+      }
+      tmem_st_x64(tmem + lane_addr + kColQ, qa);
+      tmem_st_x64(tmem + lane_addr + kColQ + 64, qb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQReady));
+    }
+    float m_ref = -INFINITY;
+    float l = 0.f;      // sum of the fp32 probabilities: gives the LSE
+    float lr = 0.f;     // rounding residuals of the blocks' largest P
+    const int key_lim = p.causal ? min(p.N_kv - 1, row) : p.N_kv - 1;   // last key this row sees
+    for (int j = 0; j < n && ok; ++j) {
+      const int b = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + b), (j >> 1) & 1, p.ctl, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_addr + kColS + 64 * b;
+      uint32_t s[64];
+      tmem_ld_x64(tS, s);
+      const int lim = key_lim - j * kBN;
+      if (__any_sync(0xffffffffu, lim < kBN - 1)) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i > lim) s[i] = __float_as_uint(-INFINITY);
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 64; i += 8) {
+        mx[0] = max3(mx[0], __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+        mx[1] = max3(mx[1], __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+        mx[2] = max3(mx[2], __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
+        mx[3] = max3(mx[3], __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+      }
+      const float mxs = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);   // raw scores
+      const float m_blk = c * mxs;
+      const float m_new = fmaxf(m_ref, m_blk);
+      bool resc = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m_ref = m_new;
+      } else if (m_new - m_ref > p.tau) {
+        resc = true;
+        alpha = ex2_hw(m_ref - m_new);
+        l *= alpha;
+        lr *= alpha;
+        m_ref = m_new;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // P_{j-1} V_{j-1} may still be accumulating into O: wait for it (the
+        // release of V_{j-1}'s slot is committed after it)
+        const int iv = 2 * j - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVEmpty + ring_slot(iv)), ring_phase(iv), p.ctl, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + 32 * ch, o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                  make_float2(alpha, alpha));
+            o[i] = __float_as_uint(r.x);
+            o[i + 1] = __float_as_uint(r.y);
+          }
+          tmem_st_x32(tO + 32 * ch, o);
+        }
+      }
+      const float2 c2 = make_float2(c, c);
+      const float2 neg2 = make_float2(-m_ref, -m_ref);
+      float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+        const float e0 = ex2_mix<EMU>(x.x, 2 * i);
+        const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
+        sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
+        if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
+        pk[i] = pack_bf16x2(e0, e1);
+      }
+      tmem_st_x32(tS, pk);   // waits for its own stores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kPFull + b));
+      l += (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
+      {
+        // the block's largest P: with every exponential on the ex2 unit,
+        // recomputed exactly as its element was (same fused multiply-add)
+        const float pm = EMU > 0 ? pmax : ex2_hw(fmaf(mxs, c, -m_ref));
+        const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
+        lr += pmr - pm;
+      }
+    }
+    // ------------------------------------------------------------- epilogue
+    bool ready = ok && n > 0;
+    if (ready) ready = mbar_wait(bar(kOFull), 0, p.ctl, abort_flag);
+    if (__all_sync(0xffffffffu, ready)) {
+      tc_fence_after();
+      const float inv_l = 1.f / (l + lr);
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + 32 * ch, o);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row < p.N_q) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (row < p.N_q)
+        p.lse[static_cast<size_t>(bh) * p.N_q + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int EMU>
+cudaError_t launch(const FwdLaunch& a) {
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.BH = a.BH;
+  p.N_q = a.N_q;
+  p.N_kv = a.N_kv;
+  p.causal = a.causal;
+  p.n_qtiles = (a.N_q + kBM - 1) / kBM;
+  p.n_steps = (a.N_kv + kBN - 1) / kBN;
+  p.c = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.tau = a.tau;
+  p.ctl = a.ctl;
+  auto kern = fwd256_kernel<EMU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.n_qtiles) * p.BH;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  return cudaGetLastError();
+}
+
+inline cudaError_t launch_any(const FwdLaunch& a) {
+  switch (a.emu_per_32) {
+    case 0: return launch<0>(a);
+    case 8: return launch<8>(a);
+    case 16: return launch<16>(a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fwd256
+}  // namespace fa

@@ -311,7 +311,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mx[2] = max3(mx[2], __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
         mx[3] = max3(mx[3], __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
       }
-      const float m_blk = c * fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
+      const float mxs = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);   // raw scores
+      const float m_blk = c * mxs;
       const float m_new = fmaxf(m_ref, m_blk);
       bool resc = false;
       float alpha = 1.f;
@@ -342,6 +343,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-m_ref, -m_ref);
       float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
@@ -349,12 +351,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const float e0 = ex2_mix<EMU>(x.x, 2 * i);
         const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
         sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
+        if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
         const uint32_t w = pack_bf16x2(e0, e1);
         pk[i] = w;
       }
       l += (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
       {
-        const float pm = ex2_hw(m_blk - m_ref);                        // the block's largest P
+        // the block's largest P: with every exponential on the ex2 unit,
+        // recomputed exactly as its element was (same fused multiply-add)
+        const float pm = EMU > 0 ? pmax : ex2_hw(fmaf(mxs, c, -m_ref));
         const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
         lr += pmr - pm;
       }

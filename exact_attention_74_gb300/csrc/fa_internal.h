@@ -10,7 +10,8 @@
 namespace fa {
 
 struct FwdLaunch {
-  CUtensorMap tmQ, tmK, tmV;   // 3-D maps (d, N, B*H), 64 x 128 x 1 boxes, 128 B swizzle
+  CUtensorMap tmQ, tmK, tmV;   // 3-D maps (d, N, B*H), 64 x 128 x 1 boxes (K, V: 64 x 64 at d = 256),
+                               // 128 B swizzle
   void* o;
   float* lse;
   int BH, N_q, N_kv, d, causal;
@@ -23,6 +24,7 @@ struct FwdLaunch {
 
 cudaError_t launch_fwd_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_d128(const FwdLaunch& a);
+cudaError_t launch_fwd_d256(const FwdLaunch& a);   // 64-row K/V boxes
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO;   // same map shape as the forward's

@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID = 1,      /* null pointer, size < 1, causal not 0/1, bad scale */
-  FA_ERR_UNSUPPORTED = 2,  /* head dimension d not in {64, 128}; no sm_103 device */
+  FA_ERR_UNSUPPORTED = 2,  /* head dimension d not supported by the call; no sm_103 device */
   FA_ERR_ALIGN = 3,        /* a pointer not 16-byte aligned (TMA requirement) */
   FA_ERR_WORKSPACE = 4,    /* fa_bwd workspace null or smaller than required */
   FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed */
@@ -62,9 +62,12 @@ typedef void* fa_stream_t;
  *   Q   bf16 [B, H, N_q,  d]      K, V bf16 [B, H, N_kv, d]
  *   O   bf16 [B, H, N_q,  d]      (output; fully overwritten, never read)
  *   LSE fp32 [B, H, N_q]          (output; natural-log logsumexp of scale*QK^T)
- *   B, H, N_q, N_kv >= 1; d in {64, 128}; causal in {0, 1};
+ *   B, H, N_q, N_kv >= 1; d in {64, 128, 256}; causal in {0, 1};
  *   scale finite and > 0 (typically 1/sqrt(d)).
- * Returns FA_OK once the kernel is enqueued on `stream`.
+ * Returns FA_OK once the kernel is enqueued on `stream`.  (d = 256, one of
+ * the head dimensions of the sweep in "FlashAttention-3: Fast and Accurate
+ * Attention with Asynchrony and Low-precision" 実験設定, has a forward
+ * kernel of its own; the backward covers d in {64, 128}.)
  */
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
            int B, int H, int N_q, int N_kv, int d, int causal, float scale,
@@ -92,7 +95,7 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * vectors D = rowsum(dO * O) and LSE * log2(e), each [B, H, N_q rounded up
  * to a multiple of 128], then one 32-bit counter per 128-row query tile
  * [B, H, ceil(N_q / 128)]; every part is rounded up to 256 bytes.  Returns 0
- * for invalid sizes.
+ * for invalid sizes and for d = 256 (no backward).
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
 
@@ -103,7 +106,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
  *   (outputs; fully overwritten).  workspace: device memory of at least
  *   fa_bwd_workspace_bytes(...) bytes, 256-byte aligned, owned by the caller;
  *   its contents on entry are ignored (it is cleared inside the call).
- * Same size, d, causal and scale rules as fa_fwd.
+ * Same size, causal and scale rules as fa_fwd; d in {64, 128} (256:
+ * FA_ERR_UNSUPPORTED).
  */
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,

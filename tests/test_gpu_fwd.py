@@ -65,14 +65,14 @@ def _wl(B, H, N_q, N_kv, d, causal, seed=7, kind="iid"):
                               causal, 1.0 / math.sqrt(d), seed, kind)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("n", [1, 3, 17, 128, 129, 255, 256, 257, 384, 1000])
+@pytest.mark.parametrize("n", [1, 3, 17, 63, 64, 65, 128, 129, 255, 256, 257, 384, 1000])
 def test_ragged_square(torch, d, causal, n):
     full_compare(torch, _wl(1, 2, n, n, d, causal, seed=n))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("nq,nkv", [(100, 300), (300, 100), (1, 513), (513, 1), (640, 130)])
 def test_ragged_rectangular(torch, d, causal, nq, nkv):
@@ -80,7 +80,7 @@ def test_ragged_rectangular(torch, d, causal, nq, nkv):
 
 
 @pytest.mark.parametrize("emu", [0, 8, 16])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_exp_emulation_mix(torch, emu, d, causal):
     full_compare(torch, _wl(1, 2, 700, 700, d, causal, seed=emu + d), emu=emu)
@@ -88,8 +88,10 @@ def test_exp_emulation_mix(torch, emu, d, causal):
 
 @pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
 @pytest.mark.parametrize("emu", [0, 16])
-def test_rescale_threshold_on_stress_inputs(torch, tau, emu):
-    w = fa_inputs.WORKLOADS["stress_8k"].with_(B=1, H=2, N_q=1024, N_kv=1024)
+@pytest.mark.parametrize("d", [128, 256])
+def test_rescale_threshold_on_stress_inputs(torch, tau, emu, d):
+    # at d = 256 the rescale waits for the previous step's P V (queued after S)
+    w = fa_inputs.WORKLOADS["stress_8k"].with_(B=1, H=2, N_q=1024, N_kv=1024, d=d)
     full_compare(torch, w, tau=tau, emu=emu)
 
 
@@ -142,3 +144,11 @@ def test_sequence_sweep(torch, causal, idx):
 def test_stress_full_size(torch):
     w = fa_inputs.WORKLOADS["stress_8k"]
     sampled_compare(torch, w, [(0, 0), (1, 9)], 64)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_size_hdim256(torch, causal):
+    """B2 H16 N8192 d256: 16k tokens at the largest head dimension of the
+    FlashAttention-3 sweep, the launch the bench times."""
+    w = fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, causal, 1.0 / 16.0, 20267)
+    sampled_compare(torch, w, [(0, 0), (1, 15)], 48)
