@@ -128,10 +128,82 @@ __global__ void wait_timeout_kernel(DevCtl ctl) {
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, ctl, &abort_flag);
 }
 
+
+// One 128 x 128 x 128 e4m3 tile product: rows converted on the device (thread
+// r converts row r of A and of B), A in shared memory (mode 0) or tensor
+// memory (mode 1), B in shared memory, both K-major with the 128-byte swizzle
+// (one 128-byte row = 128 elements).  Writes C = A8 B8^T and A's codes.
+__global__ void __launch_bounds__(128, 1)
+mma_fp8_kernel(const float* A, const float* B, float* Cout, uint8_t* a_codes, int mode, DevCtl ctl) {
+  __shared__ __align__(1024) uint8_t sA[128 * 128];
+  __shared__ __align__(1024) uint8_t sB[128 * 128];
+  __shared__ __align__(8) uint64_t bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const int r = threadIdx.x, warp = r >> 5;
+  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+  if (r == 0) {
+    mbar_init(smem_u32(&bar_done), 1);
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  uint32_t wa[32], wb[32];
+  for (int i = 0; i < 32; ++i) {
+    const float* a = A + r * 128 + 4 * i;
+    const float* b = B + r * 128 + 4 * i;
+    wa[i] = pack_e4m3x4(a[0], a[1], a[2], a[3]);
+    wb[i] = pack_e4m3x4(b[0], b[1], b[2], b[3]);
+    reinterpret_cast<uint32_t*>(a_codes + r * 128)[i] = wa[i];
+  }
+  for (int ch = 0; ch < 8; ++ch) {          // 16-byte chunk ch of row r at ch ^ (r & 7)
+    const int pc = (ch ^ (r & 7)) * 16 + r * 128;
+    *reinterpret_cast<uint4*>(sA + pc) = make_uint4(wa[4 * ch], wa[4 * ch + 1], wa[4 * ch + 2], wa[4 * ch + 3]);
+    *reinterpret_cast<uint4*>(sB + pc) = make_uint4(wb[4 * ch], wb[4 * ch + 1], wb[4 * ch + 2], wb[4 * ch + 3]);
+  }
+  if (mode == 1) tmem_st_x32(tmem + lane_addr + 128, wa);
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (r == 0) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_e4m3(128, 128);
+    for (int k = 0; k < 4; ++k) {            // 32 elements (32 bytes) per product
+      const uint64_t bd = sdesc_sw128(smem_u32(sB) + 32 * k, 0, 1024);
+      if (mode == 1)
+        mma_ts_f8(tmem, tmem + 128 + 8 * k, bd, idesc, k > 0);
+      else
+        mma_ss_f8(tmem, sdesc_sw128(smem_u32(sA) + 32 * k, 0, 1024), bd, idesc, k > 0);
+    }
+    tc_commit(smem_u32(&bar_done));
+  }
+  __syncwarp();
+  volatile int* ab = &abort_flag;
+  if (__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done), 0, ctl, ab))) {
+    tc_fence_after();
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t v[32];
+      tmem_ld_x32(tmem + lane_addr + 32 * ch, v);
+      for (int i = 0; i < 32; ++i) Cout[r * 128 + 32 * ch + i] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 }  // namespace testing
 }  // namespace fa
 
 using namespace fa;
+
 
 extern "C" {
 
@@ -173,6 +245,17 @@ int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode, fa
   }
   kern<<<1, testing::kTileThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       tmA, tmB, static_cast<const __nv_bfloat16*>(A), C, K, mode, ctl);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_test_mma_fp8(const float* A, const float* B, float* C, unsigned char* A_codes, int mode,
+                    fa_stream_t stream) {
+  if (!A || !B || !C || !A_codes) return FA_ERR_INVALID;
+  if (mode != 0 && mode != 1) return FA_ERR_INVALID;
+  DevCtl ctl;
+  const int st = device_ctl(&ctl);
+  if (st != FA_OK) return st;
+  testing::mma_fp8_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(A, B, C, A_codes, mode, ctl);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -52,6 +52,19 @@ int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode,
                      fa_stream_t stream);
 
 /*
+ * fa_test_mma_fp8 -- C = A8 * B8^T for one 128 x 128 x 128 tile with e4m3
+ * operands (the products of the 8-bit forward path, fa_fwd_fp8).
+ *   A, B fp32 [128, 128] row-major; each row is rounded to e4m3 on the
+ *   device (nearest even, saturating to +-448) exactly as the 8-bit forward
+ *   rounds its operands, and the codes of A are written to A_codes (u8
+ *   [128, 128], the OCP e4m3 encoding).
+ *   mode 0: A from shared memory; mode 1: A from tensor memory (the P
+ *   operand's path).  C fp32 [128, 128] row-major (output).
+ */
+int fa_test_mma_fp8(const float* A, const float* B, float* C, unsigned char* A_codes, int mode,
+                    fa_stream_t stream);
+
+/*
  * fa_test_wait_timeout -- launch one CTA that waits on a barrier nothing
  * will ever arrive on, with a limit of timeout_ns; the wait runs out and the
  * kernel sets the device status to FA_ERR_TIMEOUT and returns.  Used to

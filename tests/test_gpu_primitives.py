@@ -92,3 +92,40 @@ def test_watchdog_times_out_without_hanging(torch):
     # the context is still usable
     x = torch.ones(16, device="cuda")
     assert float((x * 2).sum().item()) == 32.0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mma_fp8_tile(torch, mode):
+    """e4m3 rounding on the device (nearest even) and one kind::f8f6f4 tile
+    product, A from shared or tensor memory, against PyTorch's float8_e4m3fn
+    conversion and an fp64 product of the decoded values."""
+    rng = np.random.default_rng(811 + mode)
+    A = (rng.standard_normal((128, 128)) * np.exp(rng.uniform(-6, 5, (128, 128)))).astype(np.float32)
+    B = (rng.standard_normal((128, 128)) * 4.0).astype(np.float32)
+    A = np.clip(A, -440.0, 440.0)        # saturation is checked below, separately
+    A[0, :8] = [0.0, -0.0, 1.0, -1.0, 0.0625, 1.0 / 512, 3.0 / 1024, 448.0]
+    a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    c = torch.full((128, 128), float("nan"), device="cuda")
+    codes = torch.zeros((128, 128), dtype=torch.uint8, device="cuda")
+    assert fa.fa_test_mma_fp8(a.data_ptr(), b.data_ptr(), c.data_ptr(), codes.data_ptr(), mode, 0) == fa.FA_OK
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    ref_a = torch.from_numpy(A).to(torch.float8_e4m3fn)
+    ref_b = torch.from_numpy(B).to(torch.float8_e4m3fn)
+    got = codes.cpu()
+    assert torch.equal(got, ref_a.view(torch.uint8)), "e4m3 codes differ from float8_e4m3fn"
+    expect = ref_a.to(torch.float64).numpy() @ ref_b.to(torch.float64).numpy().T
+    out = c.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(out))
+    assert np.max(np.abs(out - expect)) <= 1e-5 * (1.0 + np.max(np.abs(expect)))
+
+
+def test_e4m3_saturates(torch):
+    A = np.zeros((128, 128), dtype=np.float32)
+    A[0, :4] = [1000.0, -1000.0, 449.0, 464.0]
+    B = np.zeros((128, 128), dtype=np.float32)
+    a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    c = torch.empty((128, 128), device="cuda")
+    codes = torch.zeros((128, 128), dtype=torch.uint8, device="cuda")
+    assert fa.fa_test_mma_fp8(a.data_ptr(), b.data_ptr(), c.data_ptr(), codes.data_ptr(), 0, 0) == fa.FA_OK
+    got = codes.cpu().numpy()[0, :4]
+    assert list(got) == [0x7E, 0xFE, 0x7E, 0x7E]      # +-448, the largest finite e4m3
