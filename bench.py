@@ -488,6 +488,7 @@ def sweep(torch, fa, dev, sh, reps=10):
         out.append({"workload": w.name, "B": w.B, "N": w.N_q, "d": w.d, "causal": w.causal, "ms": ms,
                     "tflops": w.fwd_flops() / (ms * 1e-3) / 1e12})
         del q, k, v, o, lse
+    out += sweep_fp8(torch, fa, dev, sh, reps)
     # the backward workload: B2 H16 N8192 d128 causal, both reduction orders
     w = fa_inputs.WORKLOADS["bwd_8k"]
     qb, kb, vb = fa_inputs.make_qkv(w)
@@ -518,6 +519,46 @@ def sweep(torch, fa, dev, sh, reps=10):
     return out
 
 
+FP8_SIGNS = (0x9E3779B9, 0x7F4A7C15, 0x2545F491, 0x4F6CDD1D)
+
+
+def sweep_fp8(torch, fa, dev, sh, reps=10):
+    """The 8-bit forward (fa_fwd_fp8, quantisation included) on the 4k and 16k
+    configs, with plain block quantisation and with incoherent processing.
+    TFLOPS use the same 4 N^2 d count (halved when causal) as the bf16 lines."""
+    out = []
+    wls = [fa_inputs.WORKLOADS["fwd_4k"], fa_inputs.WORKLOADS["fwd_4k_causal"]]
+    wls += [w for w in fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True) if w.N_q == 16384]
+    for w in wls:
+        qb, kb, vb = fa_inputs.make_qkv(w)
+        q, k, v = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device=dev)
+        ws_bytes = fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        for signs in (None, FP8_SIGNS):
+            def call():
+                st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   w.B, w.H, w.N_q, w.N_kv, w.d, int(w.causal), w.scale, signs,
+                                   ws.data_ptr(), ws_bytes, sh)
+                assert st == fa.FA_OK
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            out.append({"workload": "fp8_" + w.name + ("_hadamard" if signs else ""), "B": w.B, "N": w.N_q,
+                        "d": w.d, "causal": w.causal, "dtype": "e4m3", "ms": ms,
+                        "tflops": w.fwd_flops() / (ms * 1e-3) / 1e12})
+        del q, k, v, o, lse, ws
+    return out
+
+
 def run_profile_case(args):
     """fwd + bwd on one named workload, W + K times, for ncu captures (prints ms only)."""
     import torch
@@ -531,6 +572,9 @@ def run_profile_case(args):
     for i in range(args.warmup + args.steps):
         if i == args.warmup:
             e0.record()
+        if args.fp8:
+            fa.forward_fp8(q, k, v, causal=w.causal, scale=w.scale, signs=FP8_SIGNS)
+            continue
         o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
         if not args.fwd_only:
             fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, workspace=ws)
@@ -556,6 +600,7 @@ def main():
     ap.add_argument("--profile", choices=sorted(fa_inputs.WORKLOADS), default=None,
                     help="only run fwd+bwd on this workload (for profiler captures)")
     ap.add_argument("--fwd-only", action="store_true", help="with --profile: forward only")
+    ap.add_argument("--fp8", action="store_true", help="with --profile: the 8-bit forward only")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps, always
     if args.impl == "reference":

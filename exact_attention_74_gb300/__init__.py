@@ -18,7 +18,7 @@ import os
 __all__ = [
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_UNSUPPORTED", "FA_ERR_ALIGN", "FA_ERR_WORKSPACE",
     "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FAError", "library", "library_path",
-    "fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_last_device_status",
+    "fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "forward_fp8", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_last_device_status",
     "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE", "fa_bwd_ex",
     "fa_set_wait_timeout_ns", "fa_status_string", "fa_test_exp2", "fa_test_mma_tile",
     "fa_test_mma_fp8", "fa_test_wait_timeout", "forward", "backward", "EXPORTED_SYMBOLS",
@@ -38,6 +38,8 @@ _ll, _ull = ctypes.c_longlong, ctypes.c_ulonglong
 _SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _f, _i, _vp]),
+    "fa_fwd_fp8_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                     _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
@@ -91,6 +93,19 @@ def fa_fwd(Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, stream=0):
 def fa_fwd_ex(Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, tau, emu_per_32, stream=0):
     return _call("fa_fwd_ex", Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, tau,
                  emu_per_32, stream)
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, N_q, N_kv, d):
+    return _call("fa_fwd_fp8_workspace_bytes", B, H, N_q, N_kv, d)
+
+
+def fa_fwd_fp8(Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, signs, workspace, workspace_bytes,
+               stream=0):
+    """signs: None, or d/32 32-bit words (a sequence of ints, or a pointer)."""
+    if signs is not None and not isinstance(signs, (int, ctypes.c_void_p)):
+        signs = (ctypes.c_uint * len(signs))(*[int(x) & 0xffffffff for x in signs])
+    return _call("fa_fwd_fp8", Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, signs, workspace,
+                 workspace_bytes, stream)
 
 
 def fa_bwd_workspace_bytes(B, H, N_q, N_kv, d):
@@ -187,6 +202,31 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None,
                        -1 if emu_per_32 is None else int(emu_per_32), s)
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
+    return out, lse
+
+
+def forward_fp8(q, k, v, causal=False, scale=None, signs=None, out=None, lse=None, stream=None,
+                workspace=None):
+    """O, LSE on 8-bit copies of q, k, v (bf16 [B, H, N, 128] on the GPU); see fa_fwd_fp8."""
+    import torch
+    B, H, N_q, d = q.shape
+    N_kv = k.shape[2]
+    _check(q, (B, H, N_q, d), "q")
+    _check(k, (B, H, N_kv, d), "k")
+    _check(v, (B, H, N_kv, d), "v")
+    scale = d ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N_q), dtype=torch.float32, device=q.device)
+    need = fa_fwd_fp8_workspace_bytes(B, H, N_q, N_kv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N_q,
+                    N_kv, d, int(causal), scale, signs, workspace.data_ptr(), workspace.numel(),
+                    _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
     return out, lse
 
 

@@ -20,8 +20,8 @@ LIBDIR = os.path.join(HERE, "lib")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(LIBDIR, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_d256.cu", "fa_bwd.cu", "fa_testing.cu",
-           "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_d256.cu", "fa_fp8.cu", "fa_bwd.cu",
+           "fa_testing.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I" + INCLUDE, "-I" + CSRC]

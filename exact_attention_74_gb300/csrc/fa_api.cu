@@ -56,6 +56,27 @@ int check_sizes(int B, int H, int N_q, int N_kv, int d, int causal, float scale)
   return FA_OK;
 }
 
+// Workspace of fa_fwd_fp8: e4m3 copies of Q, K (rows padded to 128) and of
+// V transposed, then the fp32 multipliers, each part rounded up to 256 B.
+struct Fp8Layout {
+  size_t q8, k8, vt8, qinv, kinv, vamax, total;
+};
+
+Fp8Layout fp8_layout(int B, int H, int N_q, int N_kv) {
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t nqp = (static_cast<size_t>(N_q) + 127) / 128 * 128, nkp = (static_cast<size_t>(N_kv) + 127) / 128 * 128;
+  Fp8Layout L;
+  L.q8 = 0;
+  L.k8 = L.q8 + r256(BH * nqp * 128);
+  L.vt8 = L.k8 + r256(BH * nkp * 128);
+  L.qinv = L.vt8 + r256(BH * 128 * nkp);
+  L.kinv = L.qinv + r256(BH * (nqp / 128) * sizeof(float));
+  L.vamax = L.kinv + r256(BH * (nkp / 128) * sizeof(float));
+  L.total = L.vamax + r256(BH * sizeof(unsigned));
+  return L;
+}
+
 }  // namespace
 
 // Resolve the current device: must be compute capability 10.3 (sm_103a code
@@ -112,6 +133,22 @@ int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// 3-D map over a contiguous u8 [BH, rows, inner] tensor (inner a multiple of
+// 128): 128 x 128 x 1 boxes, 128-byte swizzle.
+int make_map_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -184,6 +221,61 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N_q,
            int N_kv, int d, int causal, float scale, fa_stream_t stream) {
   return fa_fwd_ex(Q, K, V, O, LSE, B, H, N_q, N_kv, d, causal, scale, kDefaultTau, -1, stream);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
+  if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK || d != 128) return 0;
+  return fp8_layout(B, H, N_q, N_kv).total;
+}
+
+int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N_q,
+               int N_kv, int d, int causal, float scale, const unsigned* signs, void* workspace,
+               size_t workspace_bytes, fa_stream_t stream) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID;
+  int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
+      misaligned(LSE, 4))
+    return FA_ERR_ALIGN;
+  const Fp8Layout L = fp8_layout(B, H, N_q, N_kv);
+  if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
+  if (misaligned(workspace, 256)) return FA_ERR_ALIGN;
+  Fp8Launch a;
+  st = device_ctl(&a.ctl);
+  if (st != FA_OK) return st;
+  const int BH = B * H;
+  const int nqp = (N_q + 127) / 128 * 128, nkp = (N_kv + 127) / 128 * 128;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.q8 = ws + L.q8;
+  a.k8 = ws + L.k8;
+  a.vt8 = ws + L.vt8;
+  a.qinv = reinterpret_cast<float*>(ws + L.qinv);
+  a.kinv = reinterpret_cast<float*>(ws + L.kinv);
+  a.vamax = reinterpret_cast<unsigned*>(ws + L.vamax);
+  if ((st = make_map_u8(&a.tmQ8, a.q8, 128, nqp, BH)) != FA_OK) return st;
+  if ((st = make_map_u8(&a.tmK8, a.k8, 128, nkp, BH)) != FA_OK) return st;
+  if ((st = make_map_u8(&a.tmVT8, a.vt8, nkp, 128, BH)) != FA_OK) return st;
+  a.q = Q;
+  a.k = K;
+  a.v = V;
+  a.o = O;
+  a.lse = LSE;
+  a.BH = BH;
+  a.N_q = N_q;
+  a.N_kv = N_kv;
+  a.causal = causal;
+  a.hadamard = signs != nullptr;
+  for (int i = 0; i < 4; ++i) a.signs[i] = signs ? signs[i] : 0u;
+  a.scale = scale;
+  a.tau = kDefaultTau;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_fwd_fp8(a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {

@@ -48,9 +48,35 @@ struct BwdLaunch {
 
 cudaError_t launch_bwd(const BwdLaunch& a);
 
+// The 8-bit forward (d = 128): quantisation into the workspace, then the
+// attention kernel on the e4m3 copies.
+struct Fp8Launch {
+  CUtensorMap tmQ8, tmK8, tmVT8;    // u8 maps, 128 x 128 x 1 boxes, 128 B swizzle
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  uint8_t* q8;        // [B*H, N_q padded to 128, 128]
+  uint8_t* k8;        // [B*H, N_kv padded to 128, 128]
+  uint8_t* vt8;       // [B*H, 128, N_kv padded to 128]
+  float* qinv;        // [B*H, N_q blocks]
+  float* kinv;        // [B*H, N_kv blocks]
+  unsigned* vamax;    // [B*H]
+  int BH, N_q, N_kv, causal, hadamard;
+  unsigned signs[4];
+  float scale, tau;
+  DevCtl ctl;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_fwd_fp8(const Fp8Launch& a);
+
 // Defined in fa_api.cu.
 int device_ctl(DevCtl* ctl, int* n_sms = nullptr);
 int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows = 128);
 int make_map_f32(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_cols, int box_rows);
+// 3-D map over a contiguous u8 [BH, rows, inner] tensor, 128 x 128 x 1 boxes, 128-byte swizzle.
+int make_map_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int BH);
 
 }  // namespace fa

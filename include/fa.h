@@ -90,6 +90,39 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
               float tau, int emu_per_32, fa_stream_t stream);
 
 /*
+ * fa_fwd_fp8_workspace_bytes -- bytes of device workspace fa_fwd_fp8 needs:
+ * e4m3 copies of Q and K ([B, H, N rounded up to 128, d] bytes each), of V
+ * transposed ([B, H, d, N_kv rounded up to 128]), and the fp32 block
+ * multipliers; every part rounded up to 256 bytes.  0 for invalid sizes or
+ * d != 128.
+ */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
+
+/*
+ * fa_fwd_fp8 -- forward attention on 8-bit (e4m3) copies of Q, K and V, the
+ * low-precision path of "FlashAttention-3: Fast and Accurate Attention with
+ * Asynchrony and Low-precision" 技術 3 (block quantisation and incoherent
+ * processing).
+ *   Q, K, V, O, LSE, sizes, causal, scale: as fa_fwd; d must be 128.
+ *   signs    host pointer to d/32 32-bit words, or NULL.  Not NULL: before
+ *            quantisation every row of Q and K has the channels whose bit is
+ *            set negated and is multiplied by the 128 x 128 Hadamard matrix
+ *            (the same random orthogonal matrix for Q and K, so Q K^T is
+ *            unchanged); NULL: plain block quantisation.
+ *   Quantisation: one multiplier 448 / amax per 128-row block of Q and of K
+ *   (per batch and head), one per (batch, head) for V; codes are the
+ *   products rounded to e4m3 (nearest even, saturating).  The products
+ *   accumulate in fp32; P is rounded to e4m3 for P V.  O is bf16, LSE fp32.
+ *   workspace: at least fa_fwd_fp8_workspace_bytes(...) bytes, 256-byte
+ *   aligned, owned by the caller; rewritten by the call.
+ * Returns FA_OK once the work is enqueued on `stream`.
+ */
+int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+               const unsigned int* signs, void* workspace, size_t workspace_bytes,
+               fa_stream_t stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd / fa_bwd_ex need
  * for this problem: an fp32 dQ accumulator [B, H, N_q, d], then two fp32 row
  * vectors D = rowsum(dO * O) and LSE * log2(e), each [B, H, N_q rounded up

@@ -186,3 +186,36 @@ def test_bwd_ex_deterministic_flag(lib):
         == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, 1, 2, 100, 90, 64, 1, 0.125, 1, P, need - 1, 0) \
         == fa.FA_ERR_WORKSPACE
+
+
+def test_fp8_workspace_bytes(lib):
+    # Q and K codes (rows padded to 128), V transposed, two fp32 multiplier
+    # vectors and the per-head V maximum, each rounded up to 256 bytes
+    B, H, nq, nk = 2, 3, 200, 130
+    r = lambda x: (x + 255) // 256 * 256
+    want = (r(6 * 256 * 128) + r(6 * 256 * 128) + r(6 * 128 * 256) + r(6 * 2 * 4) + r(6 * 2 * 4) + r(6 * 4))
+    assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 128) == want
+    assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 64) == 0
+    assert fa.fa_fwd_fp8_workspace_bytes(B, H, 0, nk, 128) == 0
+
+
+def _fp8(ws_bytes=None, **over):
+    a = dict(Q=P, K=P, V=P, O=P, LSE=P, B=1, H=2, N_q=100, N_kv=90, d=128, causal=0, scale=0.088,
+             signs=[1, 2, 3, 4], ws=P)
+    a.update(over)
+    need = fa.fa_fwd_fp8_workspace_bytes(a["B"], a["H"], a["N_q"], a["N_kv"], 128)
+    return fa.fa_fwd_fp8(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N_q"], a["N_kv"],
+                         a["d"], a["causal"], a["scale"], a["signs"], a["ws"],
+                         need if ws_bytes is None else ws_bytes, 0)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Q=None), fa.FA_ERR_INVALID), (dict(LSE=None), fa.FA_ERR_INVALID),
+    (dict(N_q=0), fa.FA_ERR_INVALID), (dict(causal=3), fa.FA_ERR_INVALID),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID), (dict(d=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED), (dict(V=P + 8), fa.FA_ERR_ALIGN),
+    (dict(ws=None), fa.FA_ERR_WORKSPACE), (dict(ws_bytes=1024), fa.FA_ERR_WORKSPACE),
+    (dict(ws=P + 128), fa.FA_ERR_ALIGN),
+])
+def test_fp8_argument_errors(lib, over, code):
+    assert _fp8(**over) == code

@@ -1,0 +1,248 @@
+"""8-bit forward parity: fa_fwd_fp8 (through the C ABI) against ``oracle/fp8.py``.
+
+Two levels, as the method has two steps ("FlashAttention-3: Fast and
+Accurate Attention with Asynchrony and Low-precision", 技術 3):
+
+* Quantisation is integer work once the fp32 products are fixed: the e4m3
+  codes of Q, K (after the sign flips and the Hadamard butterfly when signs
+  are given) and V, and their fp32 multipliers, are read back from the
+  workspace and compared bit for bit, padded rows included.
+* Attention on those codes: the kernel's scores are exact products of the
+  codes, so LSE matches the oracle's exact LSE within 1e-3.  O differs from
+  the oracle's exact O by the e4m3 rounding of P in the P V product (and the
+  bf16 output).  Per element it must lie within the worst case of that
+  rounding, and the summed squared error must not exceed the variance that
+  rounding predicts.  The derivation is in ``_p8_bounds``; a key tile of V
+  left out, or P V taken with the wrong tile, exceeds the variance test
+  tenfold or more.
+"""
+import numpy as np
+import pytest
+
+import exact_attention_74_gb300 as fa
+import fa_inputs
+from oracle import attention as orc
+from oracle import fp8 as o8
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+SIGNS = [0x9E3779B9, 0x7F4A7C15, 0x2545F491, 0x4F6CDD1D]   # any fixed 128-bit pattern
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    assert torch.cuda.is_available()
+    fa.library()
+    return torch
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def _layout(BH, N_q, N_kv):
+    """Byte offsets of the workspace parts, in the order include/fa.h gives."""
+    nqp, nkp = -(-N_q // 128) * 128, -(-N_kv // 128) * 128
+    off = {"q8": 0}
+    off["k8"] = off["q8"] + _r256(BH * nqp * D)
+    off["vt8"] = off["k8"] + _r256(BH * nkp * D)
+    off["qinv"] = off["vt8"] + _r256(BH * D * nkp)
+    off["kinv"] = off["qinv"] + _r256(BH * (nqp // 128) * 4)
+    off["vamax"] = off["kinv"] + _r256(BH * (nkp // 128) * 4)
+    off["total"] = off["vamax"] + _r256(BH * 4)
+    return off, nqp, nkp
+
+
+def run_fp8(torch, qb, kb, vb, causal, scale, signs):
+    B, H, N_q, _ = qb.shape
+    N_kv = kb.shape[2]
+    q, k, v = gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vb)
+    o = gu.Guarded((B, H, N_q, D), torch.bfloat16)
+    lse = gu.Guarded((B, H, N_q), torch.float32)
+    need = fa.fa_fwd_fp8_workspace_bytes(B, H, N_q, N_kv, D)
+    off, _, _ = _layout(B * H, N_q, N_kv)
+    assert need == off["total"]
+    ws = gu.Guarded((need,), torch.uint8)
+    ws.view.fill_(0xA5)                       # stale contents must not leak into the result
+    st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.view.data_ptr(), lse.view.data_ptr(),
+                       B, H, N_q, N_kv, D, int(causal), scale, signs, ws.view.data_ptr(), need, 0)
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    assert o.guards_intact() and lse.guards_intact() and ws.guards_intact()
+    return (gu.to_f64(o.view), lse.view.cpu().numpy().astype(np.float64), ws.view.cpu().numpy())
+
+
+def _workspace_parts(ws, BH, N_q, N_kv):
+    off, nqp, nkp = _layout(BH, N_q, N_kv)
+    take = lambda name, n, dt: ws[off[name]:off[name] + n * np.dtype(dt).itemsize].view(dt)
+    return dict(
+        q8=take("q8", BH * nqp * D, np.uint8).reshape(BH, nqp, D),
+        k8=take("k8", BH * nkp * D, np.uint8).reshape(BH, nkp, D),
+        vt8=take("vt8", BH * D * nkp, np.uint8).reshape(BH, D, nkp),
+        qinv=take("qinv", BH * nqp // 128, np.float32).reshape(BH, -1),
+        kinv=take("kinv", BH * nkp // 128, np.float32).reshape(BH, -1),
+        vamax=take("vamax", BH, np.float32))
+
+
+def _padded_codes(vals, npad):
+    BH, N, d = vals.shape
+    out = np.zeros((BH, npad, d), dtype=np.uint8)
+    out[:, :N] = o8.e4m3_codes(vals)
+    return out
+
+
+def _same_codes(got, want, what):
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (f"{what}: {len(bad)} of {got.size} differ, first at {tuple(bad[0])}: "
+                           f"{got[tuple(bad[0])]:#04x} vs {want[tuple(bad[0])]:#04x}")
+
+
+def _p8_bounds(parts, o_ref, lse_ref, causal, s_eff, bh, rows=None):
+    """Per-element worst case and per-element variance of the error that
+    rounding P to e4m3 (and O to bf16) adds, for one (batch, head).
+
+    With W_j = exp(s_j - max) the exact weights and L = sum W_j, the kernel
+    computes sum_j r(P_j) v_j / (L' ) where r is e4m3 rounding and L' is L
+    corrected by the rounding of each key tile's largest P.  Relative to the
+    row maximum a normal P is rounded by at most 2^-4 of itself and a
+    subnormal one (below 2^-6) by at most min(2^-10, W_j); so
+        |err_i| <= sum_j h_j (|v_j| + |O_i|) / (L (1 - 2^-4)) + 2^-8 |O_i|,
+    h_j = max(2^-4 W_j, 2^-10), and, rounding errors being spread uniformly
+    over +-half a step (independent across j),
+        E[err_i^2] <= sum_j e_j (|v_j| + |O_i|)^2 / L^2 + (2^-8 O_i)^2 / 3,
+    e_j = (2^-4 W_j)^2 / 3 for normal P and min(2^-10, W_j)^2 below 2^-6.
+    """
+    N_q, N_kv = parts["q8"].shape[1], parts["k8"].shape[1]
+    qd = parts["q8"][bh] / np.repeat(parts["inv_q"][bh].astype(np.float64), 128)[:N_q, None]
+    kd = parts["k8"][bh] / np.repeat(parts["inv_k"][bh].astype(np.float64), 128)[:N_kv, None]
+    vd = parts["v8"][bh] / np.float64(parts["inv_v"][bh])
+    rows = np.arange(N_q) if rows is None else rows
+    S = s_eff * qd[rows] @ kd.T
+    if causal:
+        S = np.where(np.arange(N_kv)[None, :] <= rows[:, None], S, -np.inf)
+    m = S.max(axis=1)
+    L = np.exp(lse_ref - m)
+    W = np.exp(S - m[:, None])
+    h = np.where(np.isfinite(S), np.maximum(2.0 ** -4 * W, 2.0 ** -10), 0.0)
+    e = np.where(W >= 2.0 ** -6, (2.0 ** -4 * W) ** 2 / 3, np.minimum(2.0 ** -10, W) ** 2)
+    av, ao = np.abs(vd), np.abs(o_ref)
+    worst = (h @ av + h.sum(axis=1)[:, None] * ao) / (L[:, None] * (1 - 2.0 ** -4)) \
+        + 2.0 ** -8 * ao + 1e-5
+    var = (e @ av ** 2 + 2 * ao * (e @ av) + ao ** 2 * e.sum(axis=1)[:, None]) / L[:, None] ** 2 \
+        + (2.0 ** -8 * ao) ** 2 / 3
+    return worst, var
+
+
+def _check_o_lse(o, lse, o_ref, lse_ref, worst, var, what):
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), f"{what}: non-finite output"
+    err = o - o_ref
+    e_lse = float(np.max(np.abs(lse - lse_ref)))
+    assert e_lse <= gu.LSE_MAX_ABS, f"{what}: LSE max-abs {e_lse:.3e}"
+    ratio = float(np.max(np.abs(err) / worst))
+    assert ratio <= 1.0, f"{what}: O error {ratio:.2f} x the worst case of P's rounding"
+    vr = float(np.sum(err ** 2) / np.sum(var))
+    assert vr <= 1.0, f"{what}: squared O error {vr:.2f} x the variance P's rounding predicts"
+    return e_lse, ratio, vr
+
+
+def _qkv(rng, B, H, N_q, N_kv, kind="iid"):
+    w = fa_inputs.Workload("fp8", B, H, N_q, N_kv, D, False, D ** -0.5, int(rng.integers(1 << 30)), kind)
+    return fa_inputs.make_qkv(w)
+
+
+CASES = [
+    # B, H, N_q, N_kv, causal, signs, scale
+    (1, 2, 300, 200, False, None, None),
+    (1, 2, 300, 300, True, None, None),
+    (1, 2, 300, 300, False, SIGNS, None),
+    (2, 3, 257, 700, True, SIGNS, None),
+    (1, 1, 700, 257, False, None, None),
+    (1, 1, 700, 257, True, SIGNS, None),
+    (1, 1, 1, 130, False, None, None),
+    (1, 1, 128, 128, True, SIGNS, None),
+    (1, 2, 512, 512, False, None, 0.5),      # peaked rows: P near 2^tau before rescaling
+    (1, 2, 512, 512, True, SIGNS, 2.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N_q,N_kv,causal,signs,scale", CASES)
+def test_fp8_codes_and_output(torch, B, H, N_q, N_kv, causal, signs, scale):
+    rng = np.random.default_rng(hash((B, H, N_q, N_kv, causal, signs is None)) & 0xffff)
+    qb, kb, vb = _qkv(rng, B, H, N_q, N_kv)
+    scale = D ** -0.5 if scale is None else scale
+    o, lse, ws = run_fp8(torch, qb, kb, vb, causal, scale, signs)
+    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, causal, scale, signs=signs)
+
+    BH = B * H
+    got = _workspace_parts(ws, BH, N_q, N_kv)
+    _, nqp, nkp = _layout(BH, N_q, N_kv)
+    _same_codes(got["q8"], _padded_codes(parts["q8"], nqp), "Q codes")
+    _same_codes(got["k8"], _padded_codes(parts["k8"], nkp), "K codes")
+    _same_codes(got["vt8"], _padded_codes(parts["v8"], nkp).transpose(0, 2, 1), "V^T codes")
+    assert np.array_equal(got["qinv"], parts["inv_q"]) and np.array_equal(got["kinv"], parts["inv_k"])
+    v32 = np.abs(v.astype(np.float32)).reshape(BH, -1).max(axis=1)
+    assert np.array_equal(got["vamax"], v32), "per-head max |V|"
+
+    s_eff = scale / D if signs is not None else scale
+    o2, lse2 = o.reshape(BH, N_q, D), lse.reshape(BH, N_q)
+    o_ref2, lse_ref2 = o_ref.reshape(BH, N_q, D), lse_ref.reshape(BH, N_q)
+    for bh in range(BH):
+        worst, var = _p8_bounds(parts, o_ref2[bh], lse_ref2[bh], causal, s_eff, bh)
+        _check_o_lse(o2[bh], lse2[bh], o_ref2[bh], lse_ref2[bh], worst, var, f"bh {bh}")
+
+
+def test_fp8_zero_inputs(torch):
+    """All-zero blocks take multiplier 1 and give codes +-0 (the sign flips
+    make negative zeros); O = mean of V = 0."""
+    z = np.zeros((1, 1, 200, D), dtype=np.uint16)
+    o, lse, ws = run_fp8(torch, z, z, z, False, D ** -0.5, SIGNS)
+    assert np.all(o == 0.0)
+    assert np.allclose(lse, np.log(200.0), atol=1e-5)
+    got = _workspace_parts(ws, 1, 200, 200)
+    assert np.all(got["qinv"] == 1.0) and np.all(got["kinv"] == 1.0) and np.all(got["q8"] & 0x7F == 0)
+
+
+def test_fp8_repeatable(torch):
+    rng = np.random.default_rng(77)
+    qb, kb, vb = _qkv(rng, 1, 4, 640, 640)
+    a = run_fp8(torch, qb, kb, vb, True, D ** -0.5, SIGNS)
+    b = run_fp8(torch, qb, kb, vb, True, D ** -0.5, SIGNS)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_fp8_incoherent_processing_on_outliers(torch):
+    """On inputs with rare large outliers (N(0,1) plus, with probability
+    1e-3, N(0, 100)), the kernel's error against exact attention is lower
+    with incoherent processing than without (the page's numerical-error
+    claim), and both stay within 10% relative RMS."""
+    w = fa_inputs.Workload("outlier", 1, 4, 2048, 2048, D, False, D ** -0.5, 20268, "outlier")
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    o_exact, _ = orc.attention_forward(q, k, v, causal=False, scale=w.scale)
+    o_plain, _, _ = run_fp8(torch, qb, kb, vb, False, w.scale, None)
+    o_inc, _, _ = run_fp8(torch, qb, kb, vb, False, w.scale, SIGNS)
+    e_plain, e_inc = gu.rel_rms(o_plain, o_exact), gu.rel_rms(o_inc, o_exact)
+    assert e_inc < e_plain, (e_inc, e_plain)
+    assert e_plain < 0.1
+
+
+@pytest.mark.parametrize("name", ["fwd_4k", "fwd_4k_causal"])
+def test_fp8_full_size(torch, name):
+    """The bench workload at its real size, with incoherent processing;
+    sampled rows of three heads against the oracle run on those heads."""
+    w = fa_inputs.WORKLOADS[name]
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, lse, ws = run_fp8(torch, qb, kb, vb, w.causal, w.scale, SIGNS)
+    rng = np.random.default_rng(5)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1), (1, 7)):
+        q, k, v = (fa_inputs.bf16_bits_to_f64(x[b:b + 1, h:h + 1]) for x in (qb, kb, vb))
+        rows = gu.sample_rows(w.N_q, 48, rng)
+        o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, w.causal, w.scale, signs=SIGNS)
+        worst, var = _p8_bounds(parts, o_ref[0, 0][rows], lse_ref[0, 0][rows], w.causal, w.scale / D, 0,
+                                rows=rows)
+        _check_o_lse(o[b, h][rows], lse[b, h][rows], o_ref[0, 0][rows], lse_ref[0, 0][rows], worst, var,
+                     f"{name} b{b} h{h}")
