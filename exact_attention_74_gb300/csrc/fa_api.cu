@@ -56,10 +56,11 @@ int check_sizes(int B, int H, int N_q, int N_kv, int d, int causal, float scale)
   return FA_OK;
 }
 
-// Workspace of fa_fwd_fp8: e4m3 copies of Q, K (rows padded to 128) and of
-// V transposed, then the fp32 multipliers, each part rounded up to 256 B.
+// Workspace of fa_fwd_fp8: e4m3 copies of Q, K and V (rows padded to 128),
+// then the fp32 multipliers of Q and K, the largest |V| of each key block and
+// of each (batch, head); each part rounded up to 256 B.
 struct Fp8Layout {
-  size_t q8, k8, vt8, qinv, kinv, vamax, total;
+  size_t q8, k8, v8, qinv, kinv, vbmax, vamax, total;
 };
 
 Fp8Layout fp8_layout(int B, int H, int N_q, int N_kv) {
@@ -69,11 +70,12 @@ Fp8Layout fp8_layout(int B, int H, int N_q, int N_kv) {
   Fp8Layout L;
   L.q8 = 0;
   L.k8 = L.q8 + r256(BH * nqp * 128);
-  L.vt8 = L.k8 + r256(BH * nkp * 128);
-  L.qinv = L.vt8 + r256(BH * 128 * nkp);
+  L.v8 = L.k8 + r256(BH * nkp * 128);
+  L.qinv = L.v8 + r256(BH * nkp * 128);
   L.kinv = L.qinv + r256(BH * (nqp / 128) * sizeof(float));
-  L.vamax = L.kinv + r256(BH * (nkp / 128) * sizeof(float));
-  L.total = L.vamax + r256(BH * sizeof(unsigned));
+  L.vbmax = L.kinv + r256(BH * (nkp / 128) * sizeof(float));
+  L.vamax = L.vbmax + r256(BH * (nkp / 128) * sizeof(float));
+  L.total = L.vamax + r256(BH * sizeof(float));
   return L;
 }
 
@@ -249,13 +251,14 @@ int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.q8 = ws + L.q8;
   a.k8 = ws + L.k8;
-  a.vt8 = ws + L.vt8;
+  a.v8 = ws + L.v8;
   a.qinv = reinterpret_cast<float*>(ws + L.qinv);
   a.kinv = reinterpret_cast<float*>(ws + L.kinv);
-  a.vamax = reinterpret_cast<unsigned*>(ws + L.vamax);
+  a.vbmax = reinterpret_cast<float*>(ws + L.vbmax);
+  a.vamax = reinterpret_cast<float*>(ws + L.vamax);
   if ((st = make_map_u8(&a.tmQ8, a.q8, 128, nqp, BH)) != FA_OK) return st;
   if ((st = make_map_u8(&a.tmK8, a.k8, 128, nkp, BH)) != FA_OK) return st;
-  if ((st = make_map_u8(&a.tmVT8, a.vt8, nkp, 128, BH)) != FA_OK) return st;
+  if ((st = make_map_u8(&a.tmV8, a.v8, 128, nkp, BH)) != FA_OK) return st;
   a.q = Q;
   a.k = K;
   a.v = V;

@@ -7,16 +7,14 @@ cudaError_t launch_fwd_fp8(const Fp8Launch& a) {
   using namespace fwd8;
   const int nqb = (a.N_q + kBM - 1) / kBM, nkb = (a.N_kv + kBN - 1) / kBN;
   if (nqb > 65535 || nkb > 65535) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(a.vamax, 0, sizeof(unsigned) * a.BH, a.stream);
-  if (e != cudaSuccess) return e;
   const uint4 signs = make_uint4(a.signs[0], a.signs[1], a.signs[2], a.signs[3]);
-  quant_qk_kernel<<<dim3(a.BH, nqb > nkb ? nqb : nkb, 2), 128, 0, a.stream>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.q8, a.k8, a.qinv,
-      a.kinv, a.N_q, a.N_kv, a.hadamard, signs);
-  v_amax_kernel<<<dim3(a.BH, nkb), 128, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.v), a.vamax, a.N_kv);
-  quant_v_kernel<<<dim3(a.BH, nkb), 128, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.v), a.vamax, a.vt8,
-                                                        a.N_kv);
-  e = cudaGetLastError();
+  quant_qk_kernel<<<dim3(a.BH, nqb > nkb ? nqb : nkb, 3), kQThreads, 0, a.stream>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+      static_cast<const __nv_bfloat16*>(a.v), a.q8, a.k8, a.qinv, a.kinv, a.vbmax, a.N_q, a.N_kv, a.hadamard,
+      signs);
+  quant_v_kernel<<<dim3(a.BH, nkb), kQThreads, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.v), a.vbmax,
+                                                              a.vamax, a.v8, a.N_kv);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -38,7 +36,7 @@ cudaError_t launch_fwd_fp8(const Fp8Launch& a) {
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_qpairs) * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  fwd8_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(a.tmQ8, a.tmK8, a.tmVT8, p);
+  fwd8_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(a.tmQ8, a.tmK8, a.tmV8, p);
   return cudaGetLastError();
 }
 

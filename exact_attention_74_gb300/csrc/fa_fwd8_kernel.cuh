@@ -7,15 +7,16 @@
 // matrix D H (D random signs, H the Hadamard matrix), which leaves Q K^T
 // unchanged and spreads outlier channels ("incoherent processing").  Here:
 //
-//   quant_qk_kernel  one 128-row block of Q or K per CTA, one row per thread:
-//                    negate the channels whose sign bit is set, the Hadamard
-//                    butterfly (stages 1, 2, ..., 64, fp32, unnormalised, so
-//                    the logit scale is divided by 128), the block's largest
-//                    magnitude amax, multiplier inv = 448 / amax, codes
-//                    e4m3(x * inv) (nearest even, saturating)
-//   v_amax_kernel    the largest |V| of each (batch, head)
-//   quant_v_kernel   V's codes with that head's multiplier, written transposed
-//                    ([B*H, d, keys]) so that V is the K-major operand of P V
+//   quant_qk_kernel  one 128-row block of Q or K per CTA (four threads per
+//                    row): negate the channels whose sign bit is set, the
+//                    Hadamard butterfly (stages 1, 2, ..., 64, fp32,
+//                    unnormalised, so the logit scale is divided by 128), the
+//                    block's largest magnitude amax, multiplier
+//                    inv = 448 / amax, codes e4m3(x * inv) (nearest even,
+//                    saturating); in the same launch, each block of V's
+//                    largest |V|
+//   quant_v_kernel   V's codes with its (batch, head)'s multiplier, rows in
+//                    place ([B*H, keys, d]: the MN-major operand of P V)
 //   fwd8_kernel      the d = 128 forward of fa_fwd_kernel.cuh on e4m3 tiles
 //                    (16 KB each): kind::f8f6f4 products, S scaled by
 //                    c = scale log2(e) / (inv_q inv_k) per key tile, P rounded
@@ -57,14 +58,23 @@ __device__ constexpr uint32_t col_O(int t) { return 256u + 128u * t; }
 constexpr uint32_t kTmemCols = 512;
 
 // ------------------------------------------------------------ quantisation
+//
+// One CTA per 128-row block, four threads per row: thread (row r, quarter q)
+// holds channels 32q .. 32q + 31, so a warp loads and stores eight whole
+// rows.  The Hadamard stages h = 1 .. 16 stay inside a thread; h = 32 and 64
+// pair a thread with lane ^ 1 and lane ^ 2.
+constexpr int kQThreads = 512;
+constexpr int kQCh = 32;               // channels per thread
 
-// Largest value of v over the 128 threads of the block (all threads get it).
-__device__ __forceinline__ float block_max128(float v, float* red) {
+// Largest value of v over the 512 threads of the block (all threads get it).
+__device__ __forceinline__ float block_max512(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  v = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  v = red[0];
+#pragma unroll
+  for (int w = 1; w < kQThreads / 32; ++w) v = fmaxf(v, red[w]);
   __syncthreads();
   return v;
 }
@@ -73,9 +83,10 @@ __device__ __forceinline__ float e4m3_multiplier(float amax) {
   return amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
 }
 
-__device__ __forceinline__ void load_row_f32(const __nv_bfloat16* row, bool valid, float (&x)[D]) {
+// Channels 32q .. 32q + 31 of a row as fp32 (zeros when !valid).
+__device__ __forceinline__ void load_quarter(const __nv_bfloat16* row, bool valid, float (&x)[kQCh]) {
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i) {
+  for (int i = 0; i < kQCh / 8; ++i) {
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if (valid) w = reinterpret_cast<const uint4*>(row)[i];
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -87,98 +98,104 @@ __device__ __forceinline__ void load_row_f32(const __nv_bfloat16* row, bool vali
   }
 }
 
-// grid (B*H, blocks, 2): z = 0 quantises Q, z = 1 K.  Rows past N are zeros.
-__global__ void __launch_bounds__(128)
+__device__ __forceinline__ float max_abs(const float (&x)[kQCh]) {
+  float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < kQCh; ++c) m = fmaxf(m, fabsf(x[c]));
+  return m;
+}
+
+// Codes of x * inv, stored as 32 bytes at dst (16-byte aligned).
+__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&x)[kQCh], float inv, bool valid) {
+  uint32_t w[kQCh / 4];
+#pragma unroll
+  for (int i = 0; i < kQCh / 4; ++i)
+    w[i] = valid ? pack_e4m3x4(__fmul_rn(x[4 * i], inv), __fmul_rn(x[4 * i + 1], inv),
+                               __fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv))
+                 : 0u;     // rows past N: +0 codes
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// grid (B*H, blocks, 3): z = 0 quantises a block of Q, z = 1 of K (after
+// the sign flips and the Hadamard transform when hadamard != 0); z = 2
+// writes the largest |V| of a block of V to vbmax.  Rows past N count as
+// zeros.
+__global__ void __launch_bounds__(kQThreads)
 quant_qk_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
-                uint8_t* __restrict__ Q8, uint8_t* __restrict__ K8, float* __restrict__ qinv,
-                float* __restrict__ kinv, int N_q, int N_kv, int hadamard, uint4 signs) {
-  __shared__ float red[4];
-  const bool is_k = blockIdx.z == 1;
-  const int N = is_k ? N_kv : N_q;
+                const __nv_bfloat16* __restrict__ V, uint8_t* __restrict__ Q8, uint8_t* __restrict__ K8,
+                float* __restrict__ qinv, float* __restrict__ kinv, float* __restrict__ vbmax, int N_q,
+                int N_kv, int hadamard, uint4 signs) {
+  __shared__ float red[kQThreads / 32];
+  const int z = blockIdx.z;
+  const int N = z == 0 ? N_q : N_kv;
   const int nblk = (N + kBM - 1) / kBM;
   const int blk = blockIdx.y;
   if (blk >= nblk) return;                              // uniform over the block
   const int bh = blockIdx.x;
-  const int r = blk * kBM + threadIdx.x;
-  const __nv_bfloat16* src = (is_k ? K : Q) + (static_cast<size_t>(bh) * N + r) * D;
-  float x[D];
-  load_row_f32(src, r < N, x);
+  const int q = threadIdx.x & 3;
+  const int r = blk * kBM + (threadIdx.x >> 2);
+  const bool valid = r < N;
+  const __nv_bfloat16* src = z == 0 ? Q : z == 1 ? K : V;
+  float x[kQCh];
+  load_quarter(src + (static_cast<size_t>(bh) * N + r) * D + kQCh * q, valid, x);
+  if (z == 2) {
+    const float m = block_max512(max_abs(x), red);
+    if (threadIdx.x == 0) vbmax[static_cast<size_t>(bh) * nblk + blk] = m;
+    return;
+  }
   if (hadamard) {
-    const uint32_t sw[4] = {signs.x, signs.y, signs.z, signs.w};
+    const uint32_t sw = q == 0 ? signs.x : q == 1 ? signs.y : q == 2 ? signs.z : signs.w;
 #pragma unroll
-    for (int c = 0; c < D; ++c)
-      x[c] *= ((sw[c >> 5] >> (c & 31)) & 1u) ? -1.f : 1.f;
+    for (int c = 0; c < kQCh; ++c)
+      if ((sw >> c) & 1u) x[c] = -x[c];
 #pragma unroll
-    for (int h = 1; h < D; h *= 2) {
+    for (int h = 1; h < kQCh; h *= 2) {
 #pragma unroll
-      for (int i = 0; i < D; ++i) {
+      for (int i = 0; i < kQCh; ++i) {
         if (i & h) continue;
         const float a = x[i], b = x[i + h];
         x[i] = __fadd_rn(a, b);
         x[i + h] = __fsub_rn(a, b);
       }
     }
+#pragma unroll
+    for (int s = 1; s <= 2; s <<= 1) {                  // h = 32 (lane ^ 1), h = 64 (lane ^ 2)
+      const bool lower = (q & s) == 0;
+#pragma unroll
+      for (int c = 0; c < kQCh; ++c) {
+        const float y = __shfl_xor_sync(0xffffffffu, x[c], s);
+        x[c] = lower ? __fadd_rn(x[c], y) : __fsub_rn(y, x[c]);
+      }
+    }
   }
-  float m = 0.f;
-#pragma unroll
-  for (int c = 0; c < D; ++c) m = fmaxf(m, fabsf(x[c]));
-  const float inv = e4m3_multiplier(block_max128(m, red));
-  // rows past N are written as +0 codes (the sign flips would leave -0 in
-  // some channels, which is the same value but not the same byte)
-  uint32_t codes[D / 4];
-#pragma unroll
-  for (int i = 0; i < D / 4; ++i)
-    codes[i] = r < N ? pack_e4m3x4(__fmul_rn(x[4 * i], inv), __fmul_rn(x[4 * i + 1], inv),
-                                   __fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv))
-                     : 0u;
+  const float inv = e4m3_multiplier(block_max512(max_abs(x), red));
   const size_t npad = static_cast<size_t>(nblk) * kBM;
-  uint4* dst = reinterpret_cast<uint4*>((is_k ? K8 : Q8) + (static_cast<size_t>(bh) * npad + r) * D);
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
-  if (threadIdx.x == 0) (is_k ? kinv : qinv)[static_cast<size_t>(bh) * nblk + blk] = inv;
+  store_codes((z == 1 ? K8 : Q8) + (static_cast<size_t>(bh) * npad + r) * D + kQCh * q, x, inv, valid);
+  if (threadIdx.x == 0) (z == 1 ? kinv : qinv)[static_cast<size_t>(bh) * nblk + blk] = inv;
 }
 
-// grid (B*H, key blocks): the largest |V| of each (batch, head), as the bits
-// of a non-negative float (which order like unsigned integers).
-__global__ void __launch_bounds__(128)
-v_amax_kernel(const __nv_bfloat16* __restrict__ V, unsigned* __restrict__ vamax, int N_kv) {
-  __shared__ float red[4];
+// grid (B*H, key blocks): V's codes with its head's multiplier 448 / max|V|
+// (the maximum of the head's block maxima), rows in place ([B*H, keys padded
+// to 128, d]); block 0 also stores that maximum in vamax for the epilogue.
+__global__ void __launch_bounds__(kQThreads)
+quant_v_kernel(const __nv_bfloat16* __restrict__ V, const float* __restrict__ vbmax,
+               float* __restrict__ vamax, uint8_t* __restrict__ V8, int N_kv) {
+  __shared__ float red[kQThreads / 32];
   const int bh = blockIdx.x;
-  const int r = blockIdx.y * kBM + threadIdx.x;
-  float x[D];
-  load_row_f32(V + (static_cast<size_t>(bh) * N_kv + r) * D, r < N_kv, x);
+  const int nblk = gridDim.y;
   float m = 0.f;
-#pragma unroll
-  for (int c = 0; c < D; ++c) m = fmaxf(m, fabsf(x[c]));
-  m = block_max128(m, red);
-  if (threadIdx.x == 0) atomicMax(vamax + bh, __float_as_uint(m));
-}
-
-// grid (B*H, key blocks): codes of V with its head's multiplier, transposed
-// through shared memory into VT8 [B*H, d, keys padded to 128].
-__global__ void __launch_bounds__(128)
-quant_v_kernel(const __nv_bfloat16* __restrict__ V, const unsigned* __restrict__ vamax,
-               uint8_t* __restrict__ VT8, int N_kv) {
-  __shared__ __align__(16) uint8_t tile[D * kBN];        // [d][key in block]
-  const int bh = blockIdx.x;
-  const int t = threadIdx.x;
-  const int r = blockIdx.y * kBN + t;
-  const float inv = e4m3_multiplier(__uint_as_float(vamax[bh]));
-  float x[D];
-  load_row_f32(V + (static_cast<size_t>(bh) * N_kv + r) * D, r < N_kv, x);
-#pragma unroll
-  for (int i = 0; i < D / 4; ++i) {
-    const uint32_t w = pack_e4m3x4(__fmul_rn(x[4 * i], inv), __fmul_rn(x[4 * i + 1], inv),
-                                   __fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv));
-#pragma unroll
-    for (int e = 0; e < 4; ++e) tile[(4 * i + e) * kBN + t] = static_cast<uint8_t>(w >> (8 * e));
-  }
-  __syncthreads();
-  const size_t npad = static_cast<size_t>(gridDim.y) * kBN;
-  uint4* dst = reinterpret_cast<uint4*>(VT8 + (static_cast<size_t>(bh) * D + t) * npad + blockIdx.y * kBN);
-  const uint4* srow = reinterpret_cast<const uint4*>(tile + t * kBN);
-#pragma unroll
-  for (int i = 0; i < kBN / 16; ++i) dst[i] = srow[i];
+  for (int i = threadIdx.x; i < nblk; i += kQThreads) m = fmaxf(m, vbmax[static_cast<size_t>(bh) * nblk + i]);
+  m = block_max512(m, red);
+  if (blockIdx.y == 0 && threadIdx.x == 0) vamax[bh] = m;
+  const int q = threadIdx.x & 3;
+  const int r = blockIdx.y * kBN + (threadIdx.x >> 2);
+  const bool valid = r < N_kv;
+  float x[kQCh];
+  load_quarter(V + (static_cast<size_t>(bh) * N_kv + r) * D + kQCh * q, valid, x);
+  const size_t npad = static_cast<size_t>(nblk) * kBN;
+  store_codes(V8 + (static_cast<size_t>(bh) * npad + r) * D + kQCh * q, x, e4m3_multiplier(m), valid);
 }
 
 // ----------------------------------------------------------------- forward
@@ -188,7 +205,7 @@ struct Params {
   float* lse;
   const float* qinv;       // [B*H, q blocks]
   const float* kinv;       // [B*H, key blocks]
-  const unsigned* vamax;   // [B*H]
+  const float* vamax;      // [B*H] largest |V|
   int BH, N_q, N_kv, causal;
   int n_qpairs, n_qblk, n_kv_tiles;
   float c0;                // scale * log2(e) (/ 128 with the Hadamard transform)
@@ -212,7 +229,7 @@ __device__ __forceinline__ float e4m3_value(float x) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-            const __grid_constant__ CUtensorMap tmVT, const Params p) {
+            const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -261,7 +278,7 @@ fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (lane == 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
-      tma_prefetch_map(&tmVT);
+      tma_prefetch_map(&tmV);
       for (int t = 0; t < 2; ++t) {
         if (n_t[t] == 0) continue;
         mbar_arrive_expect_tx(bar(kQFull + t), kTileBytes);
@@ -275,10 +292,7 @@ fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           if (!mbar_wait(bar(kKVEmpty + slot), ph ^ 1, p.ctl, abort_flag)) goto producer_done;
           const uint32_t dst = sb + kKVOff + slot * kTileBytes;
           mbar_arrive_expect_tx(bar(kKVFull + slot), kTileBytes);
-          if (kind == 0)
-            tma_load_3d_hint(dst, &tmK, bar(kKVFull + slot), 0, j * kBN, bh, keep);
-          else    // V^T tile: 128 keys (x) of the 128 channel rows
-            tma_load_3d_hint(dst, &tmVT, bar(kKVFull + slot), j * kBN, 0, bh, keep);
+          tma_load_3d_hint(dst, kind == 0 ? &tmK : &tmV, bar(kKVFull + slot), 0, j * kBN, bh, keep);
           if (++slot == kSlots) { slot = 0; ph ^= 1; }
         }
       }
@@ -287,7 +301,8 @@ fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3(kBM, kBN);   // N = 128 for both products (d = 128)
+      constexpr uint32_t idesc = idesc_e4m3(kBM, kBN);           // S = Q K^T, both K-major
+      constexpr uint32_t idesc_pv = idesc_e4m3(kBM, D, true);    // O += P V, V MN-major
       auto issue_S = [&](int t, int kslot, auto&& peek) {
         const uint32_t qa = sb + kQOff + t * kTileBytes;
         const uint32_t ka = sb + kKVOff + kslot * kTileBytes;
@@ -302,7 +317,9 @@ fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const uint32_t va = sb + kKVOff + vslot * kTileBytes;
 #pragma unroll
         for (int k = 0; k < kBN / 32; ++k)
-          mma_ts_f8(tmem + col_O(t), tmem + col_S(t) + 8 * k, sdesc_sw128(va + 32 * k, 0, 1024), idesc,
+          // 32 keys = 32 rows of 128 bytes per product; the tile is one
+          // 128-byte panel wide, so both offsets are the 8-row stride
+          mma_ts_f8(tmem + col_O(t), tmem + col_S(t) + 8 * k, sdesc_sw128(va + 4096 * k, 1024, 1024), idesc_pv,
                     (acc || k > 0) ? 1u : 0u);
       };
       // K_j and V_j are ring loads 2j and 2j+1; the softmax warps release them
@@ -459,7 +476,7 @@ fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (ready) ready = mbar_wait(bar(kOFull + t), 0, p.ctl, abort_flag);
     if (__all_sync(0xffffffffu, ready)) {
       tc_fence_after();
-      const float vinv = e4m3_multiplier(__uint_as_float(p.vamax[bh]));
+      const float vinv = e4m3_multiplier(p.vamax[bh]);
       const float inv_l = 1.f / ((l + lr) * vinv);
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
 #pragma unroll

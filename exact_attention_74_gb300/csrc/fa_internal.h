@@ -51,7 +51,7 @@ cudaError_t launch_bwd(const BwdLaunch& a);
 // The 8-bit forward (d = 128): quantisation into the workspace, then the
 // attention kernel on the e4m3 copies.
 struct Fp8Launch {
-  CUtensorMap tmQ8, tmK8, tmVT8;    // u8 maps, 128 x 128 x 1 boxes, 128 B swizzle
+  CUtensorMap tmQ8, tmK8, tmV8;     // u8 maps, 128 x 128 x 1 boxes, 128 B swizzle
   const void* q;
   const void* k;
   const void* v;
@@ -59,10 +59,11 @@ struct Fp8Launch {
   float* lse;
   uint8_t* q8;        // [B*H, N_q padded to 128, 128]
   uint8_t* k8;        // [B*H, N_kv padded to 128, 128]
-  uint8_t* vt8;       // [B*H, 128, N_kv padded to 128]
+  uint8_t* v8;        // [B*H, N_kv padded to 128, 128]
   float* qinv;        // [B*H, N_q blocks]
   float* kinv;        // [B*H, N_kv blocks]
-  unsigned* vamax;    // [B*H]
+  float* vbmax;       // [B*H, N_kv blocks] largest |V| of each block
+  float* vamax;       // [B*H] largest |V| of each (batch, head)
   int BH, N_q, N_kv, causal, hadamard;
   unsigned signs[4];
   float scale, tau;

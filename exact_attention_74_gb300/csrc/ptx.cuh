@@ -296,9 +296,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 //   bit 15 A major (1 = MN), bit 16 B major, bits 17-22 N >> 3, bits 24-28 M >> 4.
 // Instruction descriptor for kind::f8f6f4 with e4m3 A and B (type code 0),
-// fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// fp32 D; A K-major, B K-major or (b_mn_major) MN-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D (+)= A * B^T with 8-bit operands, A and B from shared memory.

@@ -90,11 +90,12 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
               float tau, int emu_per_32, fa_stream_t stream);
 
 /*
- * fa_fwd_fp8_workspace_bytes -- bytes of device workspace fa_fwd_fp8 needs:
- * e4m3 copies of Q and K ([B, H, N rounded up to 128, d] bytes each), of V
- * transposed ([B, H, d, N_kv rounded up to 128]), and the fp32 block
- * multipliers; every part rounded up to 256 bytes.  0 for invalid sizes or
- * d != 128.
+ * fa_fwd_fp8_workspace_bytes -- bytes of device workspace fa_fwd_fp8 needs,
+ * in this order, each part rounded up to 256 bytes: e4m3 codes of Q, K and
+ * V ([B, H, N rounded up to 128, d] bytes each; rows past N hold +0), fp32
+ * multipliers of Q and of K ([B, H, N rounded up to 128 / 128]), the fp32
+ * largest |V| of each 128-key block ([B, H, N_kv rounded up to 128 / 128])
+ * and of each (batch, head) ([B, H]).  0 for invalid sizes or d != 128.
  */
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
 

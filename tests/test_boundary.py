@@ -189,11 +189,12 @@ def test_bwd_ex_deterministic_flag(lib):
 
 
 def test_fp8_workspace_bytes(lib):
-    # Q and K codes (rows padded to 128), V transposed, two fp32 multiplier
-    # vectors and the per-head V maximum, each rounded up to 256 bytes
+    # Q, K and V codes (rows padded to 128), the Q and K multipliers, the
+    # block and head maxima of |V|, each rounded up to 256 bytes
     B, H, nq, nk = 2, 3, 200, 130
     r = lambda x: (x + 255) // 256 * 256
-    want = (r(6 * 256 * 128) + r(6 * 256 * 128) + r(6 * 128 * 256) + r(6 * 2 * 4) + r(6 * 2 * 4) + r(6 * 4))
+    want = (r(6 * 256 * 128) + r(6 * 256 * 128) + r(6 * 256 * 128) + r(6 * 2 * 4) + r(6 * 2 * 4)
+            + r(6 * 2 * 4) + r(6 * 4))
     assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 128) == want
     assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 64) == 0
     assert fa.fa_fwd_fp8_workspace_bytes(B, H, 0, nk, 128) == 0

@@ -48,10 +48,11 @@ def _layout(BH, N_q, N_kv):
     nqp, nkp = -(-N_q // 128) * 128, -(-N_kv // 128) * 128
     off = {"q8": 0}
     off["k8"] = off["q8"] + _r256(BH * nqp * D)
-    off["vt8"] = off["k8"] + _r256(BH * nkp * D)
-    off["qinv"] = off["vt8"] + _r256(BH * D * nkp)
+    off["v8"] = off["k8"] + _r256(BH * nkp * D)
+    off["qinv"] = off["v8"] + _r256(BH * nkp * D)
     off["kinv"] = off["qinv"] + _r256(BH * (nqp // 128) * 4)
-    off["vamax"] = off["kinv"] + _r256(BH * (nkp // 128) * 4)
+    off["vbmax"] = off["kinv"] + _r256(BH * (nkp // 128) * 4)
+    off["vamax"] = off["vbmax"] + _r256(BH * (nkp // 128) * 4)
     off["total"] = off["vamax"] + _r256(BH * 4)
     return off, nqp, nkp
 
@@ -81,9 +82,10 @@ def _workspace_parts(ws, BH, N_q, N_kv):
     return dict(
         q8=take("q8", BH * nqp * D, np.uint8).reshape(BH, nqp, D),
         k8=take("k8", BH * nkp * D, np.uint8).reshape(BH, nkp, D),
-        vt8=take("vt8", BH * D * nkp, np.uint8).reshape(BH, D, nkp),
+        v8=take("v8", BH * nkp * D, np.uint8).reshape(BH, nkp, D),
         qinv=take("qinv", BH * nqp // 128, np.float32).reshape(BH, -1),
         kinv=take("kinv", BH * nkp // 128, np.float32).reshape(BH, -1),
+        vbmax=take("vbmax", BH * nkp // 128, np.float32).reshape(BH, -1),
         vamax=take("vamax", BH, np.float32))
 
 
@@ -182,10 +184,14 @@ def test_fp8_codes_and_output(torch, B, H, N_q, N_kv, causal, signs, scale):
     _, nqp, nkp = _layout(BH, N_q, N_kv)
     _same_codes(got["q8"], _padded_codes(parts["q8"], nqp), "Q codes")
     _same_codes(got["k8"], _padded_codes(parts["k8"], nkp), "K codes")
-    _same_codes(got["vt8"], _padded_codes(parts["v8"], nkp).transpose(0, 2, 1), "V^T codes")
+    _same_codes(got["v8"], _padded_codes(parts["v8"], nkp), "V codes")
     assert np.array_equal(got["qinv"], parts["inv_q"]) and np.array_equal(got["kinv"], parts["inv_k"])
-    v32 = np.abs(v.astype(np.float32)).reshape(BH, -1).max(axis=1)
-    assert np.array_equal(got["vamax"], v32), "per-head max |V|"
+    nkb = nkp // 128
+    vpad = np.zeros((BH, nkp, D), dtype=np.float32)
+    vpad[:, :N_kv] = np.abs(v.astype(np.float32)).reshape(BH, N_kv, D)
+    assert np.array_equal(got["vbmax"], vpad.reshape(BH, nkb, -1).max(axis=2)), "block max |V|"
+    assert np.array_equal(got["vamax"], vpad.reshape(BH, -1).max(axis=1)), "head max |V|"
+    assert np.array_equal(np.float32(448.0) / got["vamax"], parts["inv_v"]), "V multiplier"
 
     s_eff = scale / D if signs is not None else scale
     o2, lse2 = o.reshape(BH, N_q, D), lse.reshape(BH, N_q)
