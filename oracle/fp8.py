@@ -121,14 +121,17 @@ def quantize(x: np.ndarray, block: int | None) -> tuple[np.ndarray, np.ndarray]:
     return e4m3_round(y), (inv.reshape(BH, -1) if block is not None else inv.reshape(BH))
 
 
-def fp8_forward(q, k, v, causal: bool, scale: float, signs=None):
+def fp8_forward(q, k, v, causal: bool, scale: float, signs=None, qk_block: int | None = BLOCK):
     """O, LSE of exact attention on the 8-bit inputs, and the codes' parts.
 
     q, k, v: the bf16 inputs' values [B, H, N, d] (float64, exact).  signs:
     d/32 words for incoherent processing, or None for plain quantisation.
+    qk_block: rows per Q/K scale (128, the block quantisation), or None for
+    one scale per (batch, head) -- the per-tensor baseline of the same page's
+    error table, which the library does not implement.
     Returns (O, LSE, parts) with parts = dict of the quantised values
-    q8, k8, v8 ([B*H, N, d]) and multipliers inv_q, inv_k ([B*H, blocks]),
-    inv_v ([B*H]).
+    q8, k8, v8 ([B*H, N, d]) and multipliers inv_q, inv_k ([B*H, blocks] or
+    [B*H]), inv_v ([B*H]).
     """
     B, H, N_q, d = q.shape
     N_kv = k.shape[2]
@@ -139,11 +142,15 @@ def fp8_forward(q, k, v, causal: bool, scale: float, signs=None):
     if signs is not None:
         q32, k32 = incoherent(q32, signs), incoherent(k32, signs)
         s = scale / d                        # (Q D H)(K D H)^T = d Q K^T
-    q8, inv_q = quantize(q32, BLOCK)
-    k8, inv_k = quantize(k32, BLOCK)
+    q8, inv_q = quantize(q32, qk_block)
+    k8, inv_k = quantize(k32, qk_block)
     v8, inv_v = quantize(v32, None)
-    qd = q8 / np.repeat(inv_q.astype(np.float64), BLOCK, axis=1)[:, :N_q, None]
-    kd = k8 / np.repeat(inv_k.astype(np.float64), BLOCK, axis=1)[:, :N_kv, None]
+    if qk_block is None:
+        qd = q8 / inv_q.astype(np.float64)[:, None, None]
+        kd = k8 / inv_k.astype(np.float64)[:, None, None]
+    else:
+        qd = q8 / np.repeat(inv_q.astype(np.float64), qk_block, axis=1)[:, :N_q, None]
+        kd = k8 / np.repeat(inv_k.astype(np.float64), qk_block, axis=1)[:, :N_kv, None]
     vd = v8 / inv_v.astype(np.float64)[:, None, None]
     o, lse = attention_forward(qd.reshape(B, H, N_q, d), kd.reshape(B, H, N_kv, d),
                                vd.reshape(B, H, N_kv, d), causal=causal, scale=s)

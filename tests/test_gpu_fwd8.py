@@ -220,20 +220,34 @@ def test_fp8_repeatable(torch):
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
-def test_fp8_incoherent_processing_on_outliers(torch):
-    """On inputs with rare large outliers (N(0,1) plus, with probability
-    1e-3, N(0, 100)), the kernel's error against exact attention is lower
-    with incoherent processing than without (the page's numerical-error
-    claim), and both stay within 10% relative RMS."""
+def test_fp8_accuracy_on_outliers(torch, capsys):
+    """The error experiment of the 8-bit method's page (数値誤差): inputs
+    N(0,1) + N(0,100) Bernoulli(0.001), RMSE of O against exact fp64
+    attention.  Measured on the kernels: bf16, 8-bit block quantisation,
+    8-bit block quantisation with incoherent processing; from the oracle's
+    definition (no kernel builds them): one scale per (batch, head), with
+    and without incoherent processing.  The claims checked are the page's
+    orderings: incoherent processing lowers the error, and the 8-bit path
+    stays far above bf16's error."""
     w = fa_inputs.Workload("outlier", 1, 4, 2048, 2048, D, False, D ** -0.5, 20268, "outlier")
     qb, kb, vb = fa_inputs.make_qkv(w)
     q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
     o_exact, _ = orc.attention_forward(q, k, v, causal=False, scale=w.scale)
-    o_plain, _, _ = run_fp8(torch, qb, kb, vb, False, w.scale, None)
-    o_inc, _, _ = run_fp8(torch, qb, kb, vb, False, w.scale, SIGNS)
-    e_plain, e_inc = gu.rel_rms(o_plain, o_exact), gu.rel_rms(o_inc, o_exact)
-    assert e_inc < e_plain, (e_inc, e_plain)
-    assert e_plain < 0.1
+    rmse = lambda o: float(np.sqrt(np.mean((o - o_exact) ** 2)))
+    o16, _ = fa.forward(gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vb), causal=False, scale=w.scale)
+    res = {
+        "bf16 kernel": rmse(gu.to_f64(o16)),
+        "e4m3 kernel, 128-row blocks": rmse(run_fp8(torch, qb, kb, vb, False, w.scale, None)[0]),
+        "e4m3 kernel, 128-row blocks + incoherent": rmse(run_fp8(torch, qb, kb, vb, False, w.scale, SIGNS)[0]),
+        "e4m3 definition, per-head scale": rmse(o8.fp8_forward(q, k, v, False, w.scale, qk_block=None)[0]),
+        "e4m3 definition, per-head scale + incoherent":
+            rmse(o8.fp8_forward(q, k, v, False, w.scale, signs=SIGNS, qk_block=None)[0]),
+    }
+    with capsys.disabled():
+        print("\nRMSE vs fp64 on outlier inputs, B1 H4 N2048 d128:", res)
+    assert res["e4m3 kernel, 128-row blocks + incoherent"] < res["e4m3 kernel, 128-row blocks"]
+    assert res["e4m3 definition, per-head scale + incoherent"] < res["e4m3 definition, per-head scale"]
+    assert res["bf16 kernel"] < 0.1 * res["e4m3 kernel, 128-row blocks + incoherent"]
 
 
 @pytest.mark.parametrize("name", ["fwd_4k", "fwd_4k_causal"])

@@ -133,3 +133,19 @@ def test_incoherent_processing_lowers_the_error_on_outlier_inputs():
     o_inc, _, _ = o8.fp8_forward(q, k, v, False, 128 ** -0.5, signs=signs)
     rmse = lambda o: float(np.sqrt(np.mean((o - o_ref) ** 2)))
     assert rmse(o_inc) < rmse(o_plain)
+
+
+def test_per_head_scale_is_one_block_spanning_the_head():
+    """qk_block=None (one scale per head) equals block quantisation with a
+    block as long as the sequence, and differs from 128-row blocks when the
+    blocks' ranges differ."""
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((1, 2, 256, 128))
+    q[:, :, 128:] *= 1e-3                     # second block far smaller than the first
+    k, v = rng.standard_normal((2, 1, 2, 256, 128))
+    o_t, lse_t, p_t = o8.fp8_forward(q, k, v, False, 0.1, qk_block=None)
+    o_b, lse_b, p_b = o8.fp8_forward(q, k, v, False, 0.1, qk_block=256)
+    assert np.array_equal(o_t, o_b) and np.array_equal(lse_t, lse_b)
+    assert np.array_equal(p_t["inv_q"], p_b["inv_q"][:, 0])
+    _, _, p_128 = o8.fp8_forward(q, k, v, False, 0.1)
+    assert not np.array_equal(p_128["q8"], p_t["q8"])
