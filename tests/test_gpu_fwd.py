@@ -117,6 +117,32 @@ def test_outlier_distribution_accuracy(torch, causal):
     print(f"outlier inputs causal={causal}: O RMSE vs fp64 {rmse:.3e}")
 
 
+def test_accuracy_report_outliers_4k(torch, capsys):
+    """The error study of the FlashAttention-3 notes (数値誤差) at the bench
+    shape B4 H16 N4096 d128, every head: RMSE of O against exact fp64
+    attention on N(0,1) + N(0,100)*Bernoulli(0.001) inputs, beside the RMSE
+    that rounding the exact O to bf16 alone gives (the floor of any bf16
+    output).  The kernel may add at most as much again as that floor."""
+    w = fa_inputs.WORKLOADS["fwd_4k"].with_(name="outlier_4k", kind="outlier", seed=20269)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, _ = run_fwd(torch, qb, kb, vb, False, w.scale)
+    se = se_floor = se_vs_rounded = 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            q, k, v = (fa_inputs.bf16_bits_to_f64(x[b, h]) for x in (qb, kb, vb))
+            o_ref, _ = oracle.head_forward(q, k, v, causal=False, scale=w.scale)
+            o_r = torch.from_numpy(o_ref).to(torch.bfloat16).double().numpy()
+            se += float(np.sum((o[b, h] - o_ref) ** 2))
+            se_floor += float(np.sum((o_r - o_ref) ** 2))
+            se_vs_rounded += float(np.sum((o[b, h] - o_r) ** 2))
+    n = o.size
+    rmse, floor, vs_r = (float(np.sqrt(x / n)) for x in (se, se_floor, se_vs_rounded))
+    with capsys.disabled():
+        print(f"\noutlier inputs B4 H16 N4096 d128: O RMSE vs fp64 {rmse:.3e}; "
+              f"bf16(exact) vs fp64 {floor:.3e}; kernel vs bf16(exact) {vs_r:.3e}")
+    assert rmse <= 2.0 * floor
+
+
 def sampled_compare(torch, w, heads, nrows, **kw):
     qb, kb, vb = fa_inputs.make_qkv(w)
     o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale, **kw)
