@@ -75,6 +75,12 @@ def _wl(B, H, N_q, N_kv, d, causal, seed=11, kind="iid"):
                               causal, 1.0 / math.sqrt(d), seed, kind)
 
 
+def test_many_heads(torch):
+    """B*H = 80,000 heads (more than a grid's y or z extent) of 5 query rows
+    and 7 keys, causal: every gradient of every head compared."""
+    full_compare(torch, _wl(2, 40000, 5, 7, 64, True, seed=42))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_tiny_d64(torch, causal):
     full_compare(torch, fa_inputs.WORKLOADS["tiny_causal" if causal else "tiny"])

@@ -117,6 +117,13 @@ def test_outlier_distribution_accuracy(torch, causal):
     print(f"outlier inputs causal={causal}: O RMSE vs fp64 {rmse:.3e}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_heads(torch, causal):
+    """B*H = 80,000 heads of 5 query rows and 7 keys, more than the 65,535 a
+    grid's y or z extent allows: every head is computed and compared."""
+    full_compare(torch, _wl(2, 40000, 5, 7, 64, causal, seed=41))
+
+
 def test_accuracy_report_outliers_4k(torch, capsys):
     """The error study of the FlashAttention-3 notes (数値誤差) at the bench
     shape B4 H16 N4096 d128, every head: RMSE of O against exact fp64

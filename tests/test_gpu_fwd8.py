@@ -250,6 +250,26 @@ def test_fp8_accuracy_on_outliers(torch, capsys):
     assert res["bf16 kernel"] < 0.1 * res["e4m3 kernel, 128-row blocks + incoherent"]
 
 
+def test_fp8_many_heads(torch):
+    """B*H = 66,000 heads of 5 rows (past the 65,535 of a grid's y or z
+    extent): codes, multipliers and outputs of heads at both ends compared."""
+    B, H, N = 2, 33000, 5
+    rng = np.random.default_rng(43)
+    qb, kb, vb = _qkv(rng, B, H, N, N)
+    o, lse, ws = run_fp8(torch, qb, kb, vb, True, D ** -0.5, SIGNS)
+    got = _workspace_parts(ws, B * H, N, N)
+    for bh in (0, 1, 65534, 65535, 65999):
+        b, h = divmod(bh, H)
+        q, k, v = (fa_inputs.bf16_bits_to_f64(x[b:b + 1, h:h + 1]) for x in (qb, kb, vb))
+        o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, True, D ** -0.5, signs=SIGNS)
+        _same_codes(got["q8"][bh:bh + 1], _padded_codes(parts["q8"], 128), f"Q codes bh {bh}")
+        _same_codes(got["k8"][bh:bh + 1], _padded_codes(parts["k8"], 128), f"K codes bh {bh}")
+        _same_codes(got["v8"][bh:bh + 1], _padded_codes(parts["v8"], 128), f"V codes bh {bh}")
+        assert got["qinv"][bh, 0] == parts["inv_q"][0, 0] and got["kinv"][bh, 0] == parts["inv_k"][0, 0]
+        worst, var = _p8_bounds(parts, o_ref[0, 0], lse_ref[0, 0], True, D ** -0.5 / D, 0)
+        _check_o_lse(o[b, h], lse[b, h], o_ref[0, 0], lse_ref[0, 0], worst, var, f"bh {bh}")
+
+
 @pytest.mark.parametrize("name", ["fwd_4k", "fwd_4k_causal"])
 def test_fp8_full_size(torch, name):
     """The bench workload at its real size, with incoherent processing;
