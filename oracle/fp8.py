@@ -1,8 +1,8 @@
 """The 8-bit forward's definition, on the CPU -- TEST INFRASTRUCTURE ONLY.
 
-Only ``tests/`` and the CPU-baseline leg of ``bench.py`` may import this
-module.  The library never calls it; it shares no code, constant or helper
-with the CUDA path.
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  The library never calls it; it shares no
+code, constant or helper with the CUDA path.
 
 Follows "FlashAttention-3: Fast and Accurate Attention with Asynchrony and
 Low-precision" (notes.yuuk.io), 技術 3: Q, K and V are held in 8-bit floating
