@@ -201,6 +201,26 @@ def test_fp8_codes_and_output(torch, B, H, N_q, N_kv, causal, signs, scale):
         _check_o_lse(o2[bh], lse2[bh], o_ref2[bh], lse_ref2[bh], worst, var, f"bh {bh}")
 
 
+@pytest.mark.parametrize("signs", [None, SIGNS], ids=["plain", "incoherent"])
+def test_fp8_stress_inputs(torch, signs):
+    """The rescaling stress recipe (outlier channels x20 in Q and K, a logit
+    drift of 256 across the keys, causal): the running maximum keeps rising,
+    so the O rescale and the normaliser's residuals run, and logits reach
+    hundreds, where the LSE tests the fp32 accumulation of the 8-bit scores."""
+    w = fa_inputs.Workload("fp8_stress", 1, 2, 1024, 1024, D, True, D ** -0.5, 20270, "stress")
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, lse, ws = run_fp8(torch, qb, kb, vb, True, w.scale, signs)
+    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, True, w.scale, signs=signs)
+    got = _workspace_parts(ws, 2, 1024, 1024)
+    _same_codes(got["q8"], _padded_codes(parts["q8"], 1024), "Q codes")
+    _same_codes(got["k8"], _padded_codes(parts["k8"], 1024), "K codes")
+    s_eff = w.scale / D if signs is not None else w.scale
+    for bh in range(2):
+        worst, var = _p8_bounds(parts, o_ref[0, bh], lse_ref[0, bh], True, s_eff, bh)
+        _check_o_lse(o[0, bh], lse[0, bh], o_ref[0, bh], lse_ref[0, bh], worst, var, f"bh {bh}")
+
+
 def test_fp8_zero_inputs(torch):
     """All-zero blocks take multiplier 1 and give codes +-0 (the sign flips
     make negative zeros); O = mean of V = 0."""
