@@ -519,7 +519,7 @@ def sweep(torch, fa, dev, sh, reps=10):
     return out
 
 
-FP8_SIGNS = (0x9E3779B9, 0x7F4A7C15, 0x2545F491, 0x4F6CDD1D)
+FP8_SIGNS = (0x9E3779B9, 0x7F4A7C15, 0x2545F491, 0x4F6CDD1D, 0x85EBCA6B, 0xC2B2AE35, 0x27D4EB2F, 0x165667B1)
 
 
 def sweep_fp8(torch, fa, dev, sh, reps=10):
@@ -529,6 +529,8 @@ def sweep_fp8(torch, fa, dev, sh, reps=10):
     out = []
     wls = [fa_inputs.WORKLOADS["fwd_4k"], fa_inputs.WORKLOADS["fwd_4k_causal"]]
     wls += [w for w in fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True) if w.N_q == 16384]
+    wls += [fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, False, 1.0 / 16.0, 20267),
+            fa_inputs.Workload("hdim256_8k_causal", 2, 16, 8192, 8192, 256, True, 1.0 / 16.0, 20267)]
     for w in wls:
         qb, kb, vb = fa_inputs.make_qkv(w)
         q, k, v = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb))
@@ -536,7 +538,7 @@ def sweep_fp8(torch, fa, dev, sh, reps=10):
         lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device=dev)
         ws_bytes = fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        for signs in (None, FP8_SIGNS):
+        for signs in (None, FP8_SIGNS[:w.d // 32]):
             def call():
                 st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                    w.B, w.H, w.N_q, w.N_kv, w.d, int(w.causal), w.scale, signs,
@@ -573,7 +575,7 @@ def run_profile_case(args):
         if i == args.warmup:
             e0.record()
         if args.fp8:
-            fa.forward_fp8(q, k, v, causal=w.causal, scale=w.scale, signs=FP8_SIGNS)
+            fa.forward_fp8(q, k, v, causal=w.causal, scale=w.scale, signs=FP8_SIGNS[:w.d // 32])
             continue
         o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
         if not args.fwd_only:

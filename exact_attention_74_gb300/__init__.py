@@ -207,7 +207,9 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None,
 
 def forward_fp8(q, k, v, causal=False, scale=None, signs=None, out=None, lse=None, stream=None,
                 workspace=None):
-    """O, LSE on 8-bit copies of q, k, v (bf16 [B, H, N, 128] on the GPU); see fa_fwd_fp8."""
+    """O, LSE on 8-bit copies of q, k, v (bf16 [B, H, N, d], d in {128, 256}, on the GPU).
+
+    signs: None, or d / 32 32-bit words for incoherent processing; see fa_fwd_fp8."""
     import torch
     B, H, N_q, d = q.shape
     N_kv = k.shape[2]

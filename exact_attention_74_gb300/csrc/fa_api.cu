@@ -63,15 +63,16 @@ struct Fp8Layout {
   size_t q8, k8, v8, qinv, kinv, vbmax, vamax, total;
 };
 
-Fp8Layout fp8_layout(int B, int H, int N_q, int N_kv) {
+Fp8Layout fp8_layout(int B, int H, int N_q, int N_kv, int d) {
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t nqp = (static_cast<size_t>(N_q) + 127) / 128 * 128, nkp = (static_cast<size_t>(N_kv) + 127) / 128 * 128;
   Fp8Layout L;
   L.q8 = 0;
-  L.k8 = L.q8 + r256(BH * nqp * 128);
-  L.v8 = L.k8 + r256(BH * nkp * 128);
-  L.qinv = L.v8 + r256(BH * nkp * 128);
+  const size_t dd = static_cast<size_t>(d);
+  L.k8 = L.q8 + r256(BH * nqp * dd);
+  L.v8 = L.k8 + r256(BH * nkp * dd);
+  L.qinv = L.v8 + r256(BH * nkp * dd);
   L.kinv = L.qinv + r256(BH * (nqp / 128) * sizeof(float));
   L.vbmax = L.kinv + r256(BH * (nkp / 128) * sizeof(float));
   L.vamax = L.vbmax + r256(BH * (nkp / 128) * sizeof(float));
@@ -226,8 +227,8 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 }
 
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
-  if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK || d != 128) return 0;
-  return fp8_layout(B, H, N_q, N_kv).total;
+  if (check_sizes(B, H, N_q, N_kv, d, 0, 1.0f) != FA_OK || (d != 128 && d != 256)) return 0;
+  return fp8_layout(B, H, N_q, N_kv, d).total;
 }
 
 int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N_q,
@@ -236,11 +237,11 @@ int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID;
   int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
   if (st != FA_OK) return st;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
       misaligned(LSE, 4))
     return FA_ERR_ALIGN;
-  const Fp8Layout L = fp8_layout(B, H, N_q, N_kv);
+  const Fp8Layout L = fp8_layout(B, H, N_q, N_kv, d);
   if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
   if (misaligned(workspace, 256)) return FA_ERR_ALIGN;
   Fp8Launch a;
@@ -256,9 +257,9 @@ int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
   a.kinv = reinterpret_cast<float*>(ws + L.kinv);
   a.vbmax = reinterpret_cast<float*>(ws + L.vbmax);
   a.vamax = reinterpret_cast<float*>(ws + L.vamax);
-  if ((st = make_map_u8(&a.tmQ8, a.q8, 128, nqp, BH)) != FA_OK) return st;
-  if ((st = make_map_u8(&a.tmK8, a.k8, 128, nkp, BH)) != FA_OK) return st;
-  if ((st = make_map_u8(&a.tmV8, a.v8, 128, nkp, BH)) != FA_OK) return st;
+  if ((st = make_map_u8(&a.tmQ8, a.q8, d, nqp, BH)) != FA_OK) return st;
+  if ((st = make_map_u8(&a.tmK8, a.k8, d, nkp, BH)) != FA_OK) return st;
+  if ((st = make_map_u8(&a.tmV8, a.v8, d, nkp, BH)) != FA_OK) return st;
   a.q = Q;
   a.k = K;
   a.v = V;
@@ -268,8 +269,9 @@ int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
   a.N_q = N_q;
   a.N_kv = N_kv;
   a.causal = causal;
+  a.d = d;
   a.hadamard = signs != nullptr;
-  for (int i = 0; i < 4; ++i) a.signs[i] = signs ? signs[i] : 0u;
+  for (int i = 0; i < 8; ++i) a.signs[i] = signs && i < d / 32 ? signs[i] : 0u;
   a.scale = scale;
   a.tau = kDefaultTau;
   a.stream = static_cast<cudaStream_t>(stream);

@@ -7,10 +7,10 @@
 // matrix D H (D random signs, H the Hadamard matrix), which leaves Q K^T
 // unchanged and spreads outlier channels ("incoherent processing").  Here:
 //
-//   quant_qk_kernel  one 128-row block of Q or K per CTA (four threads per
+//   quant_qk_kernel  one 128-row block of Q or K per CTA (d / 32 threads per
 //                    row): negate the channels whose sign bit is set, the
-//                    Hadamard butterfly (stages 1, 2, ..., 64, fp32,
-//                    unnormalised, so the logit scale is divided by 128), the
+//                    Hadamard butterfly (stages 1, 2, ..., d / 2, fp32,
+//                    unnormalised, so the logit scale is divided by d), the
 //                    block's largest magnitude amax, multiplier
 //                    inv = 448 / amax, codes e4m3(x * inv) (nearest even,
 //                    saturating); in the same launch, each block of V's
@@ -59,22 +59,34 @@ constexpr uint32_t kTmemCols = 512;
 
 // ------------------------------------------------------------ quantisation
 //
-// One CTA per 128-row block, four threads per row: thread (row r, quarter q)
-// holds channels 32q .. 32q + 31, so a warp loads and stores eight whole
-// rows.  The Hadamard stages h = 1 .. 16 stay inside a thread; h = 32 and 64
-// pair a thread with lane ^ 1 and lane ^ 2.
-constexpr int kQThreads = 512;
+// One CTA per 128-row block, d / 32 threads per row: thread (row r, group q)
+// holds channels 32q .. 32q + 31, so a warp loads and stores whole rows.  The
+// Hadamard stages h = 1 .. 16 stay inside a thread; h = 32, 64, 128 pair a
+// thread with lane ^ 1, ^ 2, ^ 4 (the threads of one row are adjacent lanes).
 constexpr int kQCh = 32;               // channels per thread
 
-// Largest value of v over the 512 threads of the block (all threads get it).
-__device__ __forceinline__ float block_max512(float v, float* red) {
+template <int DQ>
+struct QuantCfg {
+  static constexpr int kPerRow = DQ / kQCh;          // threads per row
+  static constexpr int kThreads = kBM * kPerRow;     // 512 at d = 128, 1024 at d = 256
+};
+
+// Sign bits of the incoherent processing: bit c % 32 of word c / 32 negates
+// channel c (d / 32 words used).
+struct SignWords {
+  uint32_t w[8];
+};
+
+// Largest value of v over the NT threads of the block (all threads get it).
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   v = red[0];
 #pragma unroll
-  for (int w = 1; w < kQThreads / 32; ++w) v = fmaxf(v, red[w]);
+  for (int w = 1; w < NT / 32; ++w) v = fmaxf(v, red[w]);
   __syncthreads();
   return v;
 }
@@ -83,8 +95,8 @@ __device__ __forceinline__ float e4m3_multiplier(float amax) {
   return amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
 }
 
-// Channels 32q .. 32q + 31 of a row as fp32 (zeros when !valid).
-__device__ __forceinline__ void load_quarter(const __nv_bfloat16* row, bool valid, float (&x)[kQCh]) {
+// This thread's 32 channels of a row as fp32 (zeros when !valid).
+__device__ __forceinline__ void load_group(const __nv_bfloat16* row, bool valid, float (&x)[kQCh]) {
 #pragma unroll
   for (int i = 0; i < kQCh / 8; ++i) {
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -122,31 +134,33 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&x)[kQCh]
 // the sign flips and the Hadamard transform when hadamard != 0); z = 2
 // writes the largest |V| of a block of V to vbmax.  Rows past N count as
 // zeros.
-__global__ void __launch_bounds__(kQThreads)
+template <int DQ>
+__global__ void __launch_bounds__(QuantCfg<DQ>::kThreads)
 quant_qk_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                 const __nv_bfloat16* __restrict__ V, uint8_t* __restrict__ Q8, uint8_t* __restrict__ K8,
                 float* __restrict__ qinv, float* __restrict__ kinv, float* __restrict__ vbmax, int N_q,
-                int N_kv, int hadamard, uint4 signs) {
-  __shared__ float red[kQThreads / 32];
+                int N_kv, int hadamard, SignWords signs) {
+  using QC = QuantCfg<DQ>;
+  __shared__ float red[QC::kThreads / 32];
   const int z = blockIdx.z;
   const int N = z == 0 ? N_q : N_kv;
   const int nblk = (N + kBM - 1) / kBM;
   const int blk = blockIdx.y;
   if (blk >= nblk) return;                              // uniform over the block
   const int bh = blockIdx.x;
-  const int q = threadIdx.x & 3;
-  const int r = blk * kBM + (threadIdx.x >> 2);
+  const int q = threadIdx.x % QC::kPerRow;
+  const int r = blk * kBM + threadIdx.x / QC::kPerRow;
   const bool valid = r < N;
   const __nv_bfloat16* src = z == 0 ? Q : z == 1 ? K : V;
   float x[kQCh];
-  load_quarter(src + (static_cast<size_t>(bh) * N + r) * D + kQCh * q, valid, x);
+  load_group(src + (static_cast<size_t>(bh) * N + r) * DQ + kQCh * q, valid, x);
   if (z == 2) {
-    const float m = block_max512(max_abs(x), red);
+    const float m = block_max<QC::kThreads>(max_abs(x), red);
     if (threadIdx.x == 0) vbmax[static_cast<size_t>(bh) * nblk + blk] = m;
     return;
   }
   if (hadamard) {
-    const uint32_t sw = q == 0 ? signs.x : q == 1 ? signs.y : q == 2 ? signs.z : signs.w;
+    const uint32_t sw = signs.w[q];
 #pragma unroll
     for (int c = 0; c < kQCh; ++c)
       if ((sw >> c) & 1u) x[c] = -x[c];
@@ -161,7 +175,7 @@ quant_qk_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __rest
       }
     }
 #pragma unroll
-    for (int s = 1; s <= 2; s <<= 1) {                  // h = 32 (lane ^ 1), h = 64 (lane ^ 2)
+    for (int s = 1; s < QC::kPerRow; s <<= 1) {         // h = 32 s: lane ^ s
       const bool lower = (q & s) == 0;
 #pragma unroll
       for (int c = 0; c < kQCh; ++c) {
@@ -170,32 +184,34 @@ quant_qk_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __rest
       }
     }
   }
-  const float inv = e4m3_multiplier(block_max512(max_abs(x), red));
+  const float inv = e4m3_multiplier(block_max<QC::kThreads>(max_abs(x), red));
   const size_t npad = static_cast<size_t>(nblk) * kBM;
-  store_codes((z == 1 ? K8 : Q8) + (static_cast<size_t>(bh) * npad + r) * D + kQCh * q, x, inv, valid);
+  store_codes((z == 1 ? K8 : Q8) + (static_cast<size_t>(bh) * npad + r) * DQ + kQCh * q, x, inv, valid);
   if (threadIdx.x == 0) (z == 1 ? kinv : qinv)[static_cast<size_t>(bh) * nblk + blk] = inv;
 }
 
 // grid (B*H, key blocks): V's codes with its head's multiplier 448 / max|V|
 // (the maximum of the head's block maxima), rows in place ([B*H, keys padded
 // to 128, d]); block 0 also stores that maximum in vamax for the epilogue.
-__global__ void __launch_bounds__(kQThreads)
+template <int DQ>
+__global__ void __launch_bounds__(QuantCfg<DQ>::kThreads)
 quant_v_kernel(const __nv_bfloat16* __restrict__ V, const float* __restrict__ vbmax,
                float* __restrict__ vamax, uint8_t* __restrict__ V8, int N_kv) {
-  __shared__ float red[kQThreads / 32];
+  using QC = QuantCfg<DQ>;
+  __shared__ float red[QC::kThreads / 32];
   const int bh = blockIdx.x;
   const int nblk = gridDim.y;
   float m = 0.f;
-  for (int i = threadIdx.x; i < nblk; i += kQThreads) m = fmaxf(m, vbmax[static_cast<size_t>(bh) * nblk + i]);
-  m = block_max512(m, red);
+  for (int i = threadIdx.x; i < nblk; i += QC::kThreads) m = fmaxf(m, vbmax[static_cast<size_t>(bh) * nblk + i]);
+  m = block_max<QC::kThreads>(m, red);
   if (blockIdx.y == 0 && threadIdx.x == 0) vamax[bh] = m;
-  const int q = threadIdx.x & 3;
-  const int r = blockIdx.y * kBN + (threadIdx.x >> 2);
+  const int q = threadIdx.x % QC::kPerRow;
+  const int r = blockIdx.y * kBN + threadIdx.x / QC::kPerRow;
   const bool valid = r < N_kv;
   float x[kQCh];
-  load_quarter(V + (static_cast<size_t>(bh) * N_kv + r) * D + kQCh * q, valid, x);
+  load_group(V + (static_cast<size_t>(bh) * N_kv + r) * DQ + kQCh * q, valid, x);
   const size_t npad = static_cast<size_t>(nblk) * kBN;
-  store_codes(V8 + (static_cast<size_t>(bh) * npad + r) * D + kQCh * q, x, e4m3_multiplier(m), valid);
+  store_codes(V8 + (static_cast<size_t>(bh) * npad + r) * DQ + kQCh * q, x, e4m3_multiplier(m), valid);
 }
 
 // ----------------------------------------------------------------- forward

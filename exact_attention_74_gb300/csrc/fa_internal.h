@@ -57,15 +57,15 @@ struct Fp8Launch {
   const void* v;
   void* o;
   float* lse;
-  uint8_t* q8;        // [B*H, N_q padded to 128, 128]
-  uint8_t* k8;        // [B*H, N_kv padded to 128, 128]
-  uint8_t* v8;        // [B*H, N_kv padded to 128, 128]
+  uint8_t* q8;        // [B*H, N_q padded to 128, d]
+  uint8_t* k8;        // [B*H, N_kv padded to 128, d]
+  uint8_t* v8;        // [B*H, N_kv padded to 128, d]
   float* qinv;        // [B*H, N_q blocks]
   float* kinv;        // [B*H, N_kv blocks]
   float* vbmax;       // [B*H, N_kv blocks] largest |V| of each block
   float* vamax;       // [B*H] largest |V| of each (batch, head)
-  int BH, N_q, N_kv, causal, hadamard;
-  unsigned signs[4];
+  int BH, N_q, N_kv, d, causal, hadamard;   // d: 128 or 256
+  unsigned signs[8];                         // d / 32 words used
   float scale, tau;
   DevCtl ctl;
   cudaStream_t stream;

@@ -95,7 +95,8 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * V ([B, H, N rounded up to 128, d] bytes each; rows past N hold +0), fp32
  * multipliers of Q and of K ([B, H, N rounded up to 128 / 128]), the fp32
  * largest |V| of each 128-key block ([B, H, N_kv rounded up to 128 / 128])
- * and of each (batch, head) ([B, H]).  0 for invalid sizes or d != 128.
+ * and of each (batch, head) ([B, H]).  0 for invalid sizes or d not in
+ * {128, 256}.
  */
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
 
@@ -104,10 +105,13 @@ size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
  * low-precision path of "FlashAttention-3: Fast and Accurate Attention with
  * Asynchrony and Low-precision" 技術 3 (block quantisation and incoherent
  * processing).
- *   Q, K, V, O, LSE, sizes, causal, scale: as fa_fwd; d must be 128.
+ *   Q, K, V, O, LSE, sizes, causal, scale: as fa_fwd; d is 128 or 256
+ *   (else FA_ERR_UNSUPPORTED).
  *   signs    host pointer to d/32 32-bit words, or NULL.  Not NULL: before
  *            quantisation every row of Q and K has the channels whose bit is
- *            set negated and is multiplied by the 128 x 128 Hadamard matrix
+ *            set (bit c % 32 of word c / 32) negated and is multiplied by the
+ *            d x d Hadamard matrix (Sylvester order, entries +-1; the logit
+ *            scale is divided by d to match)
  *            (the same random orthogonal matrix for Q and K, so Q K^T is
  *            unchanged); NULL: plain block quantisation.
  *   Quantisation: one multiplier 448 / amax per 128-row block of Q and of K

@@ -197,6 +197,8 @@ def test_fp8_workspace_bytes(lib):
             + r(6 * 2 * 4) + r(6 * 4))
     assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 128) == want
     assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 64) == 0
+    want256 = (r(6 * 256 * 256) * 3 + r(6 * 2 * 4) * 3 + r(6 * 4))
+    assert fa.fa_fwd_fp8_workspace_bytes(B, H, nq, nk, 256) == want256
     assert fa.fa_fwd_fp8_workspace_bytes(B, H, 0, nk, 128) == 0
 
 
@@ -214,7 +216,7 @@ def _fp8(ws_bytes=None, **over):
     (dict(Q=None), fa.FA_ERR_INVALID), (dict(LSE=None), fa.FA_ERR_INVALID),
     (dict(N_q=0), fa.FA_ERR_INVALID), (dict(causal=3), fa.FA_ERR_INVALID),
     (dict(scale=-1.0), fa.FA_ERR_INVALID), (dict(d=64), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED), (dict(V=P + 8), fa.FA_ERR_ALIGN),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED), (dict(V=P + 8), fa.FA_ERR_ALIGN),
     (dict(ws=None), fa.FA_ERR_WORKSPACE), (dict(ws_bytes=1024), fa.FA_ERR_WORKSPACE),
     (dict(ws=P + 128), fa.FA_ERR_ALIGN),
 ])

@@ -29,6 +29,12 @@ pytestmark = pytest.mark.gpu
 
 D = 128
 SIGNS = [0x9E3779B9, 0x7F4A7C15, 0x2545F491, 0x4F6CDD1D]   # any fixed 128-bit pattern
+SIGNS_256 = SIGNS + [0x85EBCA6B, 0xC2B2AE35, 0x27D4EB2F, 0x165667B1]
+
+
+def signs_for(d, on=True):
+    """d / 32 sign words, or None."""
+    return (SIGNS if d == 128 else SIGNS_256) if on else None
 
 
 @pytest.fixture(scope="module")
@@ -43,13 +49,13 @@ def _r256(x):
     return (x + 255) // 256 * 256
 
 
-def _layout(BH, N_q, N_kv):
+def _layout(BH, N_q, N_kv, d=D):
     """Byte offsets of the workspace parts, in the order include/fa.h gives."""
     nqp, nkp = -(-N_q // 128) * 128, -(-N_kv // 128) * 128
     off = {"q8": 0}
-    off["k8"] = off["q8"] + _r256(BH * nqp * D)
-    off["v8"] = off["k8"] + _r256(BH * nkp * D)
-    off["qinv"] = off["v8"] + _r256(BH * nkp * D)
+    off["k8"] = off["q8"] + _r256(BH * nqp * d)
+    off["v8"] = off["k8"] + _r256(BH * nkp * d)
+    off["qinv"] = off["v8"] + _r256(BH * nkp * d)
     off["kinv"] = off["qinv"] + _r256(BH * (nqp // 128) * 4)
     off["vbmax"] = off["kinv"] + _r256(BH * (nkp // 128) * 4)
     off["vamax"] = off["vbmax"] + _r256(BH * (nkp // 128) * 4)
@@ -58,31 +64,31 @@ def _layout(BH, N_q, N_kv):
 
 
 def run_fp8(torch, qb, kb, vb, causal, scale, signs):
-    B, H, N_q, _ = qb.shape
+    B, H, N_q, d = qb.shape
     N_kv = kb.shape[2]
     q, k, v = gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vb)
-    o = gu.Guarded((B, H, N_q, D), torch.bfloat16)
+    o = gu.Guarded((B, H, N_q, d), torch.bfloat16)
     lse = gu.Guarded((B, H, N_q), torch.float32)
-    need = fa.fa_fwd_fp8_workspace_bytes(B, H, N_q, N_kv, D)
-    off, _, _ = _layout(B * H, N_q, N_kv)
+    need = fa.fa_fwd_fp8_workspace_bytes(B, H, N_q, N_kv, d)
+    off, _, _ = _layout(B * H, N_q, N_kv, d)
     assert need == off["total"]
     ws = gu.Guarded((need,), torch.uint8)
     ws.view.fill_(0xA5)                       # stale contents must not leak into the result
     st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.view.data_ptr(), lse.view.data_ptr(),
-                       B, H, N_q, N_kv, D, int(causal), scale, signs, ws.view.data_ptr(), need, 0)
+                       B, H, N_q, N_kv, d, int(causal), scale, signs, ws.view.data_ptr(), need, 0)
     assert st == fa.FA_OK, fa.fa_status_string(st)
     assert fa.fa_get_last_device_status(0) == fa.FA_OK
     assert o.guards_intact() and lse.guards_intact() and ws.guards_intact()
     return (gu.to_f64(o.view), lse.view.cpu().numpy().astype(np.float64), ws.view.cpu().numpy())
 
 
-def _workspace_parts(ws, BH, N_q, N_kv):
-    off, nqp, nkp = _layout(BH, N_q, N_kv)
+def _workspace_parts(ws, BH, N_q, N_kv, d=D):
+    off, nqp, nkp = _layout(BH, N_q, N_kv, d)
     take = lambda name, n, dt: ws[off[name]:off[name] + n * np.dtype(dt).itemsize].view(dt)
     return dict(
-        q8=take("q8", BH * nqp * D, np.uint8).reshape(BH, nqp, D),
-        k8=take("k8", BH * nkp * D, np.uint8).reshape(BH, nkp, D),
-        v8=take("v8", BH * nkp * D, np.uint8).reshape(BH, nkp, D),
+        q8=take("q8", BH * nqp * d, np.uint8).reshape(BH, nqp, d),
+        k8=take("k8", BH * nkp * d, np.uint8).reshape(BH, nkp, d),
+        v8=take("v8", BH * nkp * d, np.uint8).reshape(BH, nkp, d),
         qinv=take("qinv", BH * nqp // 128, np.float32).reshape(BH, -1),
         kinv=take("kinv", BH * nkp // 128, np.float32).reshape(BH, -1),
         vbmax=take("vbmax", BH * nkp // 128, np.float32).reshape(BH, -1),
@@ -150,52 +156,59 @@ def _check_o_lse(o, lse, o_ref, lse_ref, worst, var, what):
     return e_lse, ratio, vr
 
 
-def _qkv(rng, B, H, N_q, N_kv, kind="iid"):
-    w = fa_inputs.Workload("fp8", B, H, N_q, N_kv, D, False, D ** -0.5, int(rng.integers(1 << 30)), kind)
+def _qkv(rng, B, H, N_q, N_kv, kind="iid", d=D):
+    w = fa_inputs.Workload("fp8", B, H, N_q, N_kv, d, False, d ** -0.5, int(rng.integers(1 << 30)), kind)
     return fa_inputs.make_qkv(w)
 
 
 CASES = [
-    # B, H, N_q, N_kv, causal, signs, scale
-    (1, 2, 300, 200, False, None, None),
-    (1, 2, 300, 300, True, None, None),
-    (1, 2, 300, 300, False, SIGNS, None),
-    (2, 3, 257, 700, True, SIGNS, None),
-    (1, 1, 700, 257, False, None, None),
-    (1, 1, 700, 257, True, SIGNS, None),
-    (1, 1, 1, 130, False, None, None),
-    (1, 1, 128, 128, True, SIGNS, None),
-    (1, 2, 512, 512, False, None, 0.5),      # peaked rows: P near 2^tau before rescaling
-    (1, 2, 512, 512, True, SIGNS, 2.0),
+    # d, B, H, N_q, N_kv, causal, incoherent, scale
+    (128, 1, 2, 300, 200, False, False, None),
+    (128, 1, 2, 300, 300, True, False, None),
+    (128, 1, 2, 300, 300, False, True, None),
+    (128, 2, 3, 257, 700, True, True, None),
+    (128, 1, 1, 700, 257, False, False, None),
+    (128, 1, 1, 700, 257, True, True, None),
+    (128, 1, 1, 1, 130, False, False, None),
+    (128, 1, 1, 128, 128, True, True, None),
+    (128, 1, 2, 512, 512, False, False, 0.5),      # peaked rows: P near 2^tau before rescaling
+    (128, 1, 2, 512, 512, True, True, 2.0),
+    (256, 1, 2, 300, 200, False, False, None),
+    (256, 1, 2, 300, 300, True, True, None),
+    (256, 2, 2, 257, 700, True, False, None),
+    (256, 1, 1, 700, 257, False, True, None),
+    (256, 1, 1, 1, 130, True, True, None),
+    (256, 1, 2, 512, 512, False, True, 0.25),
 ]
 
 
-@pytest.mark.parametrize("B,H,N_q,N_kv,causal,signs,scale", CASES)
-def test_fp8_codes_and_output(torch, B, H, N_q, N_kv, causal, signs, scale):
-    rng = np.random.default_rng(hash((B, H, N_q, N_kv, causal, signs is None)) & 0xffff)
-    qb, kb, vb = _qkv(rng, B, H, N_q, N_kv)
-    scale = D ** -0.5 if scale is None else scale
+@pytest.mark.parametrize("d,B,H,N_q,N_kv,causal,incoherent,scale", CASES)
+def test_fp8_codes_and_output(torch, d, B, H, N_q, N_kv, causal, incoherent, scale):
+    rng = np.random.default_rng(hash((d, B, H, N_q, N_kv, causal, incoherent)) & 0xffff)
+    qb, kb, vb = _qkv(rng, B, H, N_q, N_kv, d=d)
+    scale = d ** -0.5 if scale is None else scale
+    signs = signs_for(d, incoherent)
     o, lse, ws = run_fp8(torch, qb, kb, vb, causal, scale, signs)
     q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
     o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, causal, scale, signs=signs)
 
     BH = B * H
-    got = _workspace_parts(ws, BH, N_q, N_kv)
-    _, nqp, nkp = _layout(BH, N_q, N_kv)
+    got = _workspace_parts(ws, BH, N_q, N_kv, d)
+    _, nqp, nkp = _layout(BH, N_q, N_kv, d)
     _same_codes(got["q8"], _padded_codes(parts["q8"], nqp), "Q codes")
     _same_codes(got["k8"], _padded_codes(parts["k8"], nkp), "K codes")
     _same_codes(got["v8"], _padded_codes(parts["v8"], nkp), "V codes")
     assert np.array_equal(got["qinv"], parts["inv_q"]) and np.array_equal(got["kinv"], parts["inv_k"])
     nkb = nkp // 128
-    vpad = np.zeros((BH, nkp, D), dtype=np.float32)
-    vpad[:, :N_kv] = np.abs(v.astype(np.float32)).reshape(BH, N_kv, D)
+    vpad = np.zeros((BH, nkp, d), dtype=np.float32)
+    vpad[:, :N_kv] = np.abs(v.astype(np.float32)).reshape(BH, N_kv, d)
     assert np.array_equal(got["vbmax"], vpad.reshape(BH, nkb, -1).max(axis=2)), "block max |V|"
     assert np.array_equal(got["vamax"], vpad.reshape(BH, -1).max(axis=1)), "head max |V|"
     assert np.array_equal(np.float32(448.0) / got["vamax"], parts["inv_v"]), "V multiplier"
 
-    s_eff = scale / D if signs is not None else scale
-    o2, lse2 = o.reshape(BH, N_q, D), lse.reshape(BH, N_q)
-    o_ref2, lse_ref2 = o_ref.reshape(BH, N_q, D), lse_ref.reshape(BH, N_q)
+    s_eff = scale / d if signs is not None else scale
+    o2, lse2 = o.reshape(BH, N_q, d), lse.reshape(BH, N_q)
+    o_ref2, lse_ref2 = o_ref.reshape(BH, N_q, d), lse_ref.reshape(BH, N_q)
     for bh in range(BH):
         worst, var = _p8_bounds(parts, o_ref2[bh], lse_ref2[bh], causal, s_eff, bh)
         _check_o_lse(o2[bh], lse2[bh], o_ref2[bh], lse_ref2[bh], worst, var, f"bh {bh}")
@@ -290,19 +303,30 @@ def test_fp8_many_heads(torch):
         _check_o_lse(o[b, h], lse[b, h], o_ref[0, 0], lse_ref[0, 0], worst, var, f"bh {bh}")
 
 
-@pytest.mark.parametrize("name", ["fwd_4k", "fwd_4k_causal"])
+FULL = {
+    "fwd_4k": fa_inputs.WORKLOADS["fwd_4k"],
+    "fwd_4k_causal": fa_inputs.WORKLOADS["fwd_4k_causal"],
+    # 16k tokens at the head dimension the 8-bit measurements of the
+    # FlashAttention-3 notes centre on
+    "hdim256_8k": fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, False, 1.0 / 16.0, 20267),
+    "hdim256_8k_causal": fa_inputs.Workload("hdim256_8k_causal", 2, 16, 8192, 8192, 256, True, 1.0 / 16.0, 20267),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
 def test_fp8_full_size(torch, name):
-    """The bench workload at its real size, with incoherent processing;
-    sampled rows of three heads against the oracle run on those heads."""
-    w = fa_inputs.WORKLOADS[name]
+    """The full-size workloads, with incoherent processing; sampled rows of
+    three heads against the oracle run on those heads."""
+    w = FULL[name]
+    signs = signs_for(w.d)
     qb, kb, vb = fa_inputs.make_qkv(w)
-    o, lse, ws = run_fp8(torch, qb, kb, vb, w.causal, w.scale, SIGNS)
+    o, lse, ws = run_fp8(torch, qb, kb, vb, w.causal, w.scale, signs)
     rng = np.random.default_rng(5)
     for b, h in ((0, 0), (w.B - 1, w.H - 1), (1, 7)):
         q, k, v = (fa_inputs.bf16_bits_to_f64(x[b:b + 1, h:h + 1]) for x in (qb, kb, vb))
         rows = gu.sample_rows(w.N_q, 48, rng)
-        o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, w.causal, w.scale, signs=SIGNS)
-        worst, var = _p8_bounds(parts, o_ref[0, 0][rows], lse_ref[0, 0][rows], w.causal, w.scale / D, 0,
+        o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, w.causal, w.scale, signs=signs)
+        worst, var = _p8_bounds(parts, o_ref[0, 0][rows], lse_ref[0, 0][rows], w.causal, w.scale / w.d, 0,
                                 rows=rows)
         _check_o_lse(o[b, h][rows], lse[b, h][rows], o_ref[0, 0][rows], lse_ref[0, 0][rows], worst, var,
                      f"{name} b{b} h{h}")
