@@ -462,8 +462,7 @@ def sweep(torch, fa, dev, sh, reps=10):
     wls += [fa_inputs.WORKLOADS["stress_8k"]]
     wls += [fa_inputs.Workload("hdim64_8k", 2, 16, 8192, 8192, 64, False, 0.125, 20266),
             fa_inputs.Workload("hdim64_8k_causal", 2, 16, 8192, 8192, 64, True, 0.125, 20266),
-            fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, False, 1.0 / 16.0, 20267),
-            fa_inputs.Workload("hdim256_8k_causal", 2, 16, 8192, 8192, 256, True, 1.0 / 16.0, 20267)]
+            fa_inputs.WORKLOADS["hdim256_8k"], fa_inputs.WORKLOADS["hdim256_8k_causal"]]
     for w in wls:
         qb, kb, vb = fa_inputs.make_qkv(w)
         q, k, v = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb))
@@ -529,8 +528,7 @@ def sweep_fp8(torch, fa, dev, sh, reps=10):
     out = []
     wls = [fa_inputs.WORKLOADS["fwd_4k"], fa_inputs.WORKLOADS["fwd_4k_causal"]]
     wls += [w for w in fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True) if w.N_q == 16384]
-    wls += [fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, False, 1.0 / 16.0, 20267),
-            fa_inputs.Workload("hdim256_8k_causal", 2, 16, 8192, 8192, 256, True, 1.0 / 16.0, 20267)]
+    wls += [fa_inputs.WORKLOADS["hdim256_8k"], fa_inputs.WORKLOADS["hdim256_8k_causal"]]
     for w in wls:
         qb, kb, vb = fa_inputs.make_qkv(w)
         q, k, v = (torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in (qb, kb, vb))

@@ -308,8 +308,8 @@ FULL = {
     "fwd_4k_causal": fa_inputs.WORKLOADS["fwd_4k_causal"],
     # 16k tokens at the head dimension the 8-bit measurements of the
     # FlashAttention-3 notes centre on
-    "hdim256_8k": fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, False, 1.0 / 16.0, 20267),
-    "hdim256_8k_causal": fa_inputs.Workload("hdim256_8k_causal", 2, 16, 8192, 8192, 256, True, 1.0 / 16.0, 20267),
+    "hdim256_8k": fa_inputs.WORKLOADS["hdim256_8k"],
+    "hdim256_8k_causal": fa_inputs.WORKLOADS["hdim256_8k_causal"],
 }
 
 
