@@ -214,34 +214,37 @@ def test_fp8_codes_and_output(torch, d, B, H, N_q, N_kv, causal, incoherent, sca
         _check_o_lse(o2[bh], lse2[bh], o_ref2[bh], lse_ref2[bh], worst, var, f"bh {bh}")
 
 
-@pytest.mark.parametrize("signs", [None, SIGNS], ids=["plain", "incoherent"])
-def test_fp8_stress_inputs(torch, signs):
+@pytest.mark.parametrize("incoherent", [False, True], ids=["plain", "incoherent"])
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp8_stress_inputs(torch, d, incoherent):
     """The rescaling stress recipe (outlier channels x20 in Q and K, a logit
     drift of 256 across the keys, causal): the running maximum keeps rising,
     so the O rescale and the normaliser's residuals run, and logits reach
     hundreds, where the LSE tests the fp32 accumulation of the 8-bit scores."""
-    w = fa_inputs.Workload("fp8_stress", 1, 2, 1024, 1024, D, True, D ** -0.5, 20270, "stress")
+    w = fa_inputs.Workload("fp8_stress", 1, 2, 1024, 1024, d, True, d ** -0.5, 20270, "stress")
+    signs = signs_for(d, incoherent)
     qb, kb, vb = fa_inputs.make_qkv(w)
     o, lse, ws = run_fp8(torch, qb, kb, vb, True, w.scale, signs)
     q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
     o_ref, lse_ref, parts = o8.fp8_forward(q, k, v, True, w.scale, signs=signs)
-    got = _workspace_parts(ws, 2, 1024, 1024)
+    got = _workspace_parts(ws, 2, 1024, 1024, d)
     _same_codes(got["q8"], _padded_codes(parts["q8"], 1024), "Q codes")
     _same_codes(got["k8"], _padded_codes(parts["k8"], 1024), "K codes")
-    s_eff = w.scale / D if signs is not None else w.scale
+    s_eff = w.scale / d if signs is not None else w.scale
     for bh in range(2):
         worst, var = _p8_bounds(parts, o_ref[0, bh], lse_ref[0, bh], True, s_eff, bh)
         _check_o_lse(o[0, bh], lse[0, bh], o_ref[0, bh], lse_ref[0, bh], worst, var, f"bh {bh}")
 
 
-def test_fp8_zero_inputs(torch):
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp8_zero_inputs(torch, d):
     """All-zero blocks take multiplier 1 and give codes +-0 (the sign flips
     make negative zeros); O = mean of V = 0."""
-    z = np.zeros((1, 1, 200, D), dtype=np.uint16)
-    o, lse, ws = run_fp8(torch, z, z, z, False, D ** -0.5, SIGNS)
+    z = np.zeros((1, 1, 200, d), dtype=np.uint16)
+    o, lse, ws = run_fp8(torch, z, z, z, False, d ** -0.5, signs_for(d))
     assert np.all(o == 0.0)
     assert np.allclose(lse, np.log(200.0), atol=1e-5)
-    got = _workspace_parts(ws, 1, 200, 200)
+    got = _workspace_parts(ws, 1, 200, 200, d)
     assert np.all(got["qinv"] == 1.0) and np.all(got["kinv"] == 1.0) and np.all(got["q8"] & 0x7F == 0)
 
 
