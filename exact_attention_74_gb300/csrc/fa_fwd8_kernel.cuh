@@ -111,20 +111,26 @@ __device__ __forceinline__ void load_group(const __nv_bfloat16* row, bool valid,
 }
 
 __device__ __forceinline__ float max_abs(const float (&x)[kQCh]) {
-  float m = 0.f;
+  float m0 = 0.f, m1 = 0.f;
 #pragma unroll
-  for (int c = 0; c < kQCh; ++c) m = fmaxf(m, fabsf(x[c]));
-  return m;
+  for (int c = 0; c < kQCh; c += 4) {
+    m0 = max3(m0, fabsf(x[c]), fabsf(x[c + 1]));
+    m1 = max3(m1, fabsf(x[c + 2]), fabsf(x[c + 3]));
+  }
+  return fmaxf(m0, m1);
 }
 
-// Codes of x * inv, stored as 32 bytes at dst (16-byte aligned).
+// Codes of x * inv (each product rounded once, as __fmul_rn), stored as 32
+// bytes at dst (16-byte aligned).
 __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&x)[kQCh], float inv, bool valid) {
   uint32_t w[kQCh / 4];
+  const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-  for (int i = 0; i < kQCh / 4; ++i)
-    w[i] = valid ? pack_e4m3x4(__fmul_rn(x[4 * i], inv), __fmul_rn(x[4 * i + 1], inv),
-                               __fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv))
-                 : 0u;     // rows past N: +0 codes
+  for (int i = 0; i < kQCh / 4; ++i) {
+    const float2 a = mul2(make_float2(x[4 * i], x[4 * i + 1]), inv2);
+    const float2 b = mul2(make_float2(x[4 * i + 2], x[4 * i + 3]), inv2);
+    w[i] = valid ? pack_e4m3x4(a.x, a.y, b.x, b.y) : 0u;     // rows past N: +0 codes
+  }
   uint4* d = reinterpret_cast<uint4*>(dst);
   d[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -164,23 +170,42 @@ quant_qk_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __rest
 #pragma unroll
     for (int c = 0; c < kQCh; ++c)
       if ((sw >> c) & 1u) x[c] = -x[c];
+    // stage h = 1: (a, b) -> (a + b, a - b), each rounded once
 #pragma unroll
-    for (int h = 1; h < kQCh; h *= 2) {
+    for (int i = 0; i < kQCh; i += 2) {
+      const float a = x[i], b = x[i + 1];
+      x[i] = __fadd_rn(a, b);
+      x[i + 1] = __fsub_rn(a, b);
+    }
+    // stages h = 2 .. 16: two neighbouring butterflies per packed pair of
+    // operations; fma(-1, b, a) is a - b rounded once
+    const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
-      for (int i = 0; i < kQCh; ++i) {
+    for (int h = 2; h < kQCh; h *= 2) {
+#pragma unroll
+      for (int i = 0; i < kQCh; i += 2) {
         if (i & h) continue;
-        const float a = x[i], b = x[i + h];
-        x[i] = __fadd_rn(a, b);
-        x[i + h] = __fsub_rn(a, b);
+        const float2 a = make_float2(x[i], x[i + 1]), b = make_float2(x[i + h], x[i + h + 1]);
+        const float2 sum = add2(a, b), dif = fma2(neg1, b, a);
+        x[i] = sum.x;
+        x[i + 1] = sum.y;
+        x[i + h] = dif.x;
+        x[i + h + 1] = dif.y;
       }
     }
+    // stages h = 32 s across lanes: the lower thread of a pair keeps x + y,
+    // the upper y - x, both as fma(+-1, x, y) rounded once
 #pragma unroll
-    for (int s = 1; s < QC::kPerRow; s <<= 1) {         // h = 32 s: lane ^ s
-      const bool lower = (q & s) == 0;
+    for (int s = 1; s < QC::kPerRow; s <<= 1) {
+      const float sg = (q & s) == 0 ? 1.f : -1.f;
+      const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-      for (int c = 0; c < kQCh; ++c) {
-        const float y = __shfl_xor_sync(0xffffffffu, x[c], s);
-        x[c] = lower ? __fadd_rn(x[c], y) : __fsub_rn(y, x[c]);
+      for (int c = 0; c < kQCh; c += 2) {
+        const float2 y = make_float2(__shfl_xor_sync(0xffffffffu, x[c], s),
+                                     __shfl_xor_sync(0xffffffffu, x[c + 1], s));
+        const float2 r = fma2(sg2, make_float2(x[c], x[c + 1]), y);
+        x[c] = r.x;
+        x[c + 1] = r.y;
       }
     }
   }
