@@ -418,6 +418,8 @@ def run_gpu(args):
     if has_bwd:
         line["bwd_deterministic_tflops"] = deterministic_bwd_tflops(torch, fa, w, q, k, v, o, do, lse,
                                                                     dq, dk, dv, ws, ws_bytes, stream)
+    if w.d in (128, 256):
+        line["fwd_fp8_tflops"] = fp8_fwd_tflops(torch, fa, w, q, k, v, stream)
     if args.sweep:
         line["sweep"] = sweep(torch, fa, dev, sh)
     if rank == 0 and not args.no_cpu_baseline:
@@ -453,6 +455,34 @@ def deterministic_bwd_tflops(torch, fa, w, q, k, v, o, do, lse, dq, dk, dv, ws, 
     e1.record(stream)
     torch.cuda.synchronize()
     return w.bwd_flops() / (e0.elapsed_time(e1) / reps * 1e-3) / 1e12
+
+
+def fp8_fwd_tflops(torch, fa, w, q, k, v, stream, reps=20):
+    """The same forward through fa_fwd_fp8 (e4m3 operands, quantisation
+    included in the timed call): plain block quantisation and with
+    incoherent processing.  Same flop count as the bf16 forward."""
+    sh = stream.cuda_stream
+    o8 = torch.empty_like(q)
+    lse8 = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device=q.device)
+    ws_bytes = fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d)
+    ws8 = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    out = {}
+    for name, signs in (("plain", None), ("incoherent", FP8_SIGNS[:w.d // 32])):
+        def call():
+            st = fa.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o8.data_ptr(), lse8.data_ptr(), w.B, w.H,
+                               w.N_q, w.N_kv, w.d, int(w.causal), w.scale, signs, ws8.data_ptr(), ws_bytes, sh)
+            if st != fa.FA_OK:
+                raise fa.FAError(st, "fa_fwd_fp8")
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = w.fwd_flops() / (e0.elapsed_time(e1) / reps * 1e-3) / 1e12
+    return out
 
 
 def sweep(torch, fa, dev, sh, reps=10):
