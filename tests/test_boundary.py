@@ -222,3 +222,10 @@ def _fp8(ws_bytes=None, **over):
 ])
 def test_fp8_argument_errors(lib, over, code):
     assert _fp8(**over) == code
+
+
+def test_fp8_signs_must_cover_d(lib):
+    # d = 256 reads 8 sign words; the binding refuses a shorter list before
+    # any call (the C side cannot know the length of a host array)
+    with pytest.raises(ValueError):
+        fa.fa_fwd_fp8(P, P, P, P, P, 1, 2, 100, 90, 256, 0, 0.06, [1, 2, 3, 4], P, 1 << 20, 0)
