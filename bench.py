@@ -490,7 +490,7 @@ def sweep(torch, fa, dev, sh, reps=10):
     out = []
     wls = fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True)
     wls += [fa_inputs.WORKLOADS["stress_8k"]]
-    wls += [fa_inputs.Workload("hdim64_8k", 2, 16, 8192, 8192, 64, False, 0.125, 20266),
+    wls += [fa_inputs.WORKLOADS["hdim64_8k"],
             fa_inputs.Workload("hdim64_8k_causal", 2, 16, 8192, 8192, 64, True, 0.125, 20266),
             fa_inputs.WORKLOADS["hdim256_8k"], fa_inputs.WORKLOADS["hdim256_8k_causal"]]
     for w in wls:

@@ -97,6 +97,7 @@ WORKLOADS = {
     "bwd_8k": _wl("bwd_8k", 2, 16, 8192, 128, True, 20265),
     # 16k tokens at head dimension 256 (FlashAttention-3's largest, where
     # its 8-bit measurements centre), scale 1/16
+    "hdim64_8k": Workload("hdim64_8k", 2, 16, 8192, 8192, 64, False, 0.125, 20266),
     "hdim256_8k": Workload("hdim256_8k", 2, 16, 8192, 8192, 256, False, 1.0 / 16.0, 20267),
     "hdim256_8k_causal": Workload("hdim256_8k_causal", 2, 16, 8192, 8192, 256, True, 1.0 / 16.0, 20267),
 }
