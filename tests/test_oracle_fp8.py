@@ -47,30 +47,41 @@ def test_e4m3_ties_to_even_and_saturates():
         [0x7E, 0xFE, 0x7E, 0x00, 0x01]
 
 
-def test_fwht_is_the_sylvester_hadamard_product():
+@pytest.mark.parametrize("d", [128, 256])
+def test_fwht_is_the_sylvester_hadamard_product(d):
     scipy_linalg = pytest.importorskip("scipy.linalg")
-    H = scipy_linalg.hadamard(128).astype(np.float64)
+    H = scipy_linalg.hadamard(d).astype(np.float64)
     rng = np.random.default_rng(6)
-    xi = rng.integers(-8, 9, size=(5, 128)).astype(np.float32)      # exact in fp32
+    xi = rng.integers(-8, 9, size=(5, d)).astype(np.float32)      # exact in fp32
     assert np.array_equal(o8.fwht_f32(xi).astype(np.float64), xi.astype(np.float64) @ H)
-    x = rng.standard_normal((7, 128)).astype(np.float32)
-    assert np.max(np.abs(o8.fwht_f32(x) - x.astype(np.float64) @ H)) < 1e-4
+    x = rng.standard_normal((7, d)).astype(np.float32)
+    assert np.max(np.abs(o8.fwht_f32(x) - x.astype(np.float64) @ H)) < 1e-4 * d / 128
 
 
-def test_incoherent_processing_keeps_qk_up_to_d():
+def test_sign_vector_reads_bit_c_of_word_c_over_32():
+    # channel 37 is bit 5 of word 1; channel 255 bit 31 of word 7
+    words = [0] * 8
+    words[1] = 1 << 5
+    words[7] = 1 << 31
+    v = o8.sign_vector(words, 256)
+    assert np.flatnonzero(v < 0).tolist() == [37, 255]
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_incoherent_processing_keeps_qk_up_to_d(d):
     rng = np.random.default_rng(7)
-    q, k = rng.standard_normal((2, 64, 128))
-    signs = rng.integers(0, 2 ** 32, size=4, dtype=np.uint64)
-    D = o8.sign_vector(signs, 128).astype(np.float64)
+    q, k = rng.standard_normal((2, 64, d))
+    signs = rng.integers(0, 2 ** 32, size=d // 32, dtype=np.uint64)
+    D = o8.sign_vector(signs, d).astype(np.float64)
     assert set(np.unique(D)) == {-1.0, 1.0}
     import scipy.linalg
-    H = scipy.linalg.hadamard(128).astype(np.float64)
-    # (Q D H)(K D H)^T = Q D H H^T D K^T = 128 Q K^T
+    H = scipy.linalg.hadamard(d).astype(np.float64)
+    # (Q D H)(K D H)^T = Q D H H^T D K^T = d Q K^T
     lhs = (q * D) @ H @ ((k * D) @ H).T
-    assert np.max(np.abs(lhs - 128.0 * q @ k.T)) < 1e-9
+    assert np.max(np.abs(lhs - d * q @ k.T)) < 1e-9 * d
     # and the oracle's fp32 path agrees up to fp32 rounding
     got = o8.incoherent(q, signs).astype(np.float64) @ o8.incoherent(k, signs).astype(np.float64).T
-    assert np.max(np.abs(got - 128.0 * q @ k.T)) / np.max(np.abs(q @ k.T)) < 1e-3
+    assert np.max(np.abs(got - d * q @ k.T)) / np.max(np.abs(q @ k.T)) < 1e-3 * d / 128
 
 
 def _exact_inputs(rng, B, H, N, d, block_scale):
@@ -101,6 +112,18 @@ def test_fp8_forward_without_rounding_is_plain_attention(causal):
     assert np.max(np.abs(o - o_ref)) < 1e-12 and np.max(np.abs(lse - lse_ref)) < 1e-12
     assert parts["inv_q"][0].tolist() == [1.0, 4.0, 32.0]
     assert parts["inv_k"][0].tolist() == [2.0, 1.0, 8.0]
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp8_forward_with_signs_uses_scale_over_d_any_d(d):
+    """As below, at both head dimensions of the 8-bit path."""
+    rng = np.random.default_rng(12)
+    q, k, v = (rng.standard_normal((1, 1, 160, d)) for _ in range(3))
+    signs = rng.integers(0, 2 ** 32, size=d // 32, dtype=np.uint64)
+    o, lse, _ = o8.fp8_forward(q, k, v, False, d ** -0.5, signs=signs)
+    o_ref, lse_ref = orc.attention_forward(q, k, v, causal=False, scale=d ** -0.5)
+    assert np.max(np.abs(lse - lse_ref)) < 0.05
+    assert np.sqrt(np.mean((o - o_ref) ** 2)) / np.sqrt(np.mean(o_ref ** 2)) < 0.1
 
 
 def test_fp8_forward_with_signs_uses_scale_over_d():
