@@ -97,6 +97,35 @@ struct Params {
   DevCtl ctl;
 };
 
+// CTA b -> (key tile j, batch*head).  Head-major: the CTAs resident at one
+// time cover only a few heads, so their fp32 dQ accumulators (and Q, dO
+// tiles) stay in L2; within a head, key tile 0 runs first (with a causal
+// mask it sees the most query tiles).  In deterministic mode each query tile
+// takes its partials in decreasing key-tile order, so key tiles run from the
+// last one (a CTA then only waits for CTAs dispatched before it).  Without
+// a mask every query tile takes all key tiles' partials, so a head's CTAs
+// running side by side would each wait on the one just ahead: a group of
+// kDetGroup heads is interleaved key tile by key tile, so one wave holds a
+// few consecutive key tiles of each head of the group and most of a CTA's
+// predecessors finished a wave earlier.  (With a causal mask the later key
+// tiles see fewer query tiles and finish early by themselves.)
+constexpr int kDetGroup = 16;
+
+__device__ __forceinline__ void block_tile(const Params& p, int b, int& j, int& bh) {
+  if (!p.deterministic || p.causal) {
+    const int jj = b % p.n_kv_tiles;
+    j = p.deterministic ? p.n_kv_tiles - 1 - jj : jj;
+    bh = b / p.n_kv_tiles;
+    return;
+  }
+  const int per_group = kDetGroup * p.n_kv_tiles;
+  const int g = b / per_group;
+  const int rem = b - g * per_group;
+  const int heads = min(kDetGroup, p.BH - g * kDetGroup);   // the last group may be smaller
+  j = p.n_kv_tiles - 1 - rem / heads;
+  bh = g * kDetGroup + rem % heads;
+}
+
 // ------------------------------------------------------------------- prep
 
 template <int D>
@@ -183,15 +212,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Head-major order: the CTAs resident at one time cover only a few heads,
-  // so their fp32 dQ accumulators (and Q, dO tiles) stay in L2.  Within a
-  // head, key tile 0 runs first: with a causal mask it sees the most query
-  // tiles.  In deterministic mode each query tile takes its partials in
-  // decreasing key-tile order, so key tiles are launched from the last one:
-  // a CTA then only waits for CTAs dispatched before it.
-  const int jj = static_cast<int>(blockIdx.x) % p.n_kv_tiles;
-  const int j = p.deterministic ? p.n_kv_tiles - 1 - jj : jj;
-  const int bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
+  int j, bh;
+  block_tile(p, static_cast<int>(blockIdx.x), j, bh);
   const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
   const int n_it = max(0, p.n_q_tiles - i0);
 
@@ -272,9 +294,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           // K/V tile nobody has touched yet: start it towards L2 now.
           const int nb = static_cast<int>(blockIdx.x) + p.n_sms;
           if (nb < static_cast<int>(gridDim.x)) {
-            const int njj = nb % p.n_kv_tiles;
-            const int nj = p.deterministic ? p.n_kv_tiles - 1 - njj : njj;
-            const int nbh = nb / p.n_kv_tiles;
+            int nj, nbh;
+            block_tile(p, nb, nj, nbh);
             for (int pn = 0; pn < D / 64; ++pn) {
               tma_prefetch_l2_3d(&tmK, pn * 64, nj * kBM, nbh);
               tma_prefetch_l2_3d(&tmV, pn * 64, nj * kBM, nbh);
