@@ -111,10 +111,11 @@ struct Params {
 // tiles see fewer query tiles and finish early by themselves.)
 constexpr int kDetGroup = 16;
 
+template <bool DET>
 __device__ __forceinline__ void block_tile(const Params& p, int b, int& j, int& bh) {
-  if (!p.deterministic || p.causal) {
+  if (!DET || p.causal) {
     const int jj = b % p.n_kv_tiles;
-    j = p.deterministic ? p.n_kv_tiles - 1 - jj : jj;
+    j = DET ? p.n_kv_tiles - 1 - jj : jj;
     bh = b / p.n_kv_tiles;
     return;
   }
@@ -194,7 +195,9 @@ convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, lo
 
 // ------------------------------------------------------------------- main
 
-template <int D>
+// DET: the fixed-order (bit-reproducible) dQ reduction, compiled as its own
+// instance so that the unordered kernel carries none of its code.
+template <int D, bool DET>
 __global__ void __launch_bounds__(kThreads, 1)
 main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -213,7 +216,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int j, bh;
-  block_tile(p, static_cast<int>(blockIdx.x), j, bh);
+  block_tile<DET>(p, static_cast<int>(blockIdx.x), j, bh);
   const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
   const int n_it = max(0, p.n_q_tiles - i0);
 
@@ -254,6 +257,17 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       }
       const uint64_t keep = l2_policy_evict_last();
       constexpr int kBoxes = D / 64;            // 32-column boxes per compute warp
+      // Fixed order: once a partial has landed, the next key tile may add
+      // into that query tile.  The landing wait is taken after this step's
+      // loads are issued, so it overlaps them instead of delaying them.
+      unsigned* release_cnt = nullptr;
+      auto release = [&] {
+        if (release_cnt == nullptr) return;
+        bulk_wait_group0();
+        fence_proxy_async_global();
+        red_release_gpu_add(release_cnt, 1u);
+        release_cnt = nullptr;
+      };
       for (int t = 0; t < n_it + 2; ++t) {
         const int s = t & 1;
         if (t >= 2) {
@@ -265,7 +279,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           if (!mbar_wait(bar(C::kStagedQ + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
           const int ip = i0 + t - 2;
           unsigned* cnt = p.counters + static_cast<size_t>(bh) * p.n_q_tiles + ip;
-          if (p.deterministic) {
+          if constexpr (DET) {
             // key tiles above this one (up to the last that sees query tile ip) add first
             const int top = p.causal ? min(ip, p.n_kv_tiles - 1) : p.n_kv_tiles - 1;
             if (!wait_counter(cnt, static_cast<unsigned>(top - j), p.ctl, abort_flag)) break;
@@ -283,11 +297,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             bulk_commit_group();
           }
           if (*abort_flag) break;
-          if (p.deterministic) {                 // landed: the next key tile may add
-            bulk_wait_group0();
-            fence_proxy_async_global();
-            red_release_gpu_add(cnt, 1u);
-          }
+          if constexpr (DET) release_cnt = cnt;
         }
         if (t == max(0, n_it - 4)) {
           // The CTA that this SM (or another) runs one wave later reads a
@@ -295,14 +305,17 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           const int nb = static_cast<int>(blockIdx.x) + p.n_sms;
           if (nb < static_cast<int>(gridDim.x)) {
             int nj, nbh;
-            block_tile(p, nb, nj, nbh);
+            block_tile<DET>(p, nb, nj, nbh);
             for (int pn = 0; pn < D / 64; ++pn) {
               tma_prefetch_l2_3d(&tmK, pn * 64, nj * kBM, nbh);
               tma_prefetch_l2_3d(&tmV, pn * 64, nj * kBM, nbh);
             }
           }
         }
-        if (t >= n_it) continue;
+        if (t >= n_it) {
+          if constexpr (DET) release();
+          continue;
+        }
         const int i = i0 + t;
         if (t >= 2) bulk_wait_group_read<1>();    // Q-buffer boxes read
         const uint32_t fq = bar(C::kQFull + s);
@@ -317,7 +330,9 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         mbar_arrive_expect_tx(fd, C::kTile);
         for (int pn = 0; pn < D / 64; ++pn)
           tma_load_3d_hint(sb + C::do_off(s) + pn * kPanel, &tmdO, fd, pn * 64, i * kBN, bh, keep);
+        if constexpr (DET) release();
       }
+      if constexpr (DET) release();
       bulk_wait_group0();                       // every reduction has landed
     }
   } else if (n_it > 0 && warp == 1) {
@@ -664,7 +679,7 @@ cudaError_t launch(const BwdLaunch& a) {
   p.scale = a.scale;
   p.ctl = a.ctl;
   p.n_sms = a.n_sms;
-  auto kern = main_kernel<D>;
+  auto kern = a.deterministic ? main_kernel<D, true> : main_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_kv_tiles) * p.BH;
