@@ -209,6 +209,52 @@ def test_deterministic_bitwise_repeatable_and_exact(torch, d, causal, nq, nkv):
     check_grads([gu.to_f64(x) for x in a], ref, f"deterministic {w.name}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_deterministic_head_groups(torch, d):
+    """Without a mask the fixed-order mode dispatches heads in groups of 16,
+    interleaved key tile by key tile; 22 heads make one full group and one
+    of 6, and 700 keys six key tiles: every head compared, bit-identical
+    across calls."""
+    w = _wl(2, 11, 700, 700, d, False, seed=97 + d)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     w.B, w.H, w.N_q, w.N_kv, d, 0, w.scale, 0) == fa.FA_OK
+    t = (q, k, v, o, do, lse)
+    a = _bwd_ex(torch, w, t, 1)
+    b = _bwd_ex(torch, w, t, 1)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    ref = oracle.attention_backward(*(fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb, dob)),
+                                    causal=False, scale=w.scale)
+    check_grads([gu.to_f64(x) for x in a], ref, f"deterministic {w.name}")
+
+
+def test_deterministic_full_size_noncausal(torch):
+    """The bench workload (64 heads: four groups of 16) in the fixed-order
+    mode: bit-identical across calls, and two heads against the oracle."""
+    w = fa_inputs.WORKLOADS["fwd_4k"]
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     w.B, w.H, w.N_q, w.N_kv, w.d, 0, w.scale, 0) == fa.FA_OK
+    t = (q, k, v, o, do, lse)
+    a = _bwd_ex(torch, w, t, 1)
+    b = _bwd_ex(torch, w, t, 1)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    for bi, hi in ((0, 0), (3, 15)):
+        q64, k64, v64, do64 = (fa_inputs.bf16_bits_to_f64(x[bi, hi]) for x in (qb, kb, vb, dob))
+        ref = oracle.head_backward(q64, k64, v64, do64, causal=False, scale=w.scale)
+        check_grads([gu.to_f64(x)[bi, hi] for x in a], ref, f"deterministic fwd_4k b{bi} h{hi}")
+
+
 def test_deterministic_full_size_causal(torch):
     w = fa_inputs.WORKLOADS["bwd_8k"]
     qb, kb, vb = fa_inputs.make_qkv(w)
