@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include "fa.h"
@@ -41,11 +42,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct DevState {
   bool checked = false;
   bool supported = false;
-  unsigned* status = nullptr;
   int n_sms = 0;
 };
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+// True when p lies in memory the current device addresses directly: a device
+// allocation of this device (or one it has peer access to) or managed
+// memory.  Host memory, pinned or not, and unknown addresses are refused, so
+// no tensor map or kernel is ever built on them.
+bool is_device_memory(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeDevice && at.devicePointer != nullptr;
+}
+
+int check_device_memory(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (!is_device_memory(p)) return FA_ERR_INVALID;
+  return FA_OK;
+}
 
 int check_sizes(int B, int H, int N_q, int N_kv, int d, int causal, float scale) {
   if (B < 1 || H < 1 || N_q < 1 || N_kv < 1) return FA_ERR_INVALID;
@@ -108,18 +128,18 @@ int device_ctl(DevCtl* ctl, int* n_sms) {
       cudaGetLastError();
       return FA_ERR_CUDA;
     }
-    if (s.supported) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_CUDA;
-      }
-      s.status = static_cast<unsigned*>(p);
-    }
     s.checked = true;
   }
   if (!s.supported) return FA_ERR_UNSUPPORTED;
-  ctl->status = s.status;
+  // The status word's device address is looked up on every call (a host-side
+  // query): a context torn down and re-created (cudaDeviceReset) reloads the
+  // module, and the word may then live elsewhere.
+  void* word = nullptr;
+  if (cudaGetSymbolAddress(&word, g_status_word) != cudaSuccess || word == nullptr) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  ctl->status = static_cast<unsigned*>(word);
   ctl->timeout_ns = g_timeout_ns.load();
   if (n_sms) *n_sms = s.n_sms;
   return FA_OK;
@@ -197,6 +217,7 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
   FwdLaunch a;
   st = device_ctl(&a.ctl);
   if (st != FA_OK) return st;
+  if ((st = check_device_memory({Q, K, V, O, LSE})) != FA_OK) return st;
   const int BH = B * H;
   const int kv_rows = d == 256 ? 64 : 128;   // rows per K/V box (the d = 256 kernel steps 64 keys)
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
@@ -247,6 +268,7 @@ int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
   Fp8Launch a;
   st = device_ctl(&a.ctl);
   if (st != FA_OK) return st;
+  if ((st = check_device_memory({Q, K, V, O, LSE, workspace})) != FA_OK) return st;
   const int BH = B * H;
   const int nqp = (N_q + 127) / 128 * 128, nkp = (N_kv + 127) / 128 * 128;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -290,12 +312,20 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d) {
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
   const size_t vec = (rows_pad * sizeof(float) + 255) / 256 * 256;
   const size_t cnt = (rows_pad / 128 * sizeof(unsigned) + 255) / 256 * 256;
-  return acc + 2 * vec + cnt;
+  return acc + 2 * vec + cnt + 256;   // + the CTA ticket word
 }
 
-int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+}  // extern "C"
+
+namespace fa {
+
+// fa_bwd_ex's work; `internal_workspace` marks the library's own scratch
+// (fa_bwd_noalloc), whose address is not a caller's allocation and is not
+// checked as one.
+int bwd_entry(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
               void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
-              int deterministic, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+              int deterministic, void* workspace, size_t workspace_bytes, bool internal_workspace,
+              cudaStream_t stream) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID;
   int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
   if (st != FA_OK) return st;
@@ -311,6 +341,8 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const 
   BwdLaunch a;
   st = device_ctl(&a.ctl, &a.n_sms);
   if (st != FA_OK) return st;
+  if ((st = check_device_memory({Q, K, V, O, dO, LSE, dQ, dK, dV})) != FA_OK) return st;
+  if (!internal_workspace && (st = check_device_memory({workspace})) != FA_OK) return st;
   const int BH = B * H;
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH)) != FA_OK) return st;
@@ -330,6 +362,8 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const 
                                      (rows * d * sizeof(float) + 255) / 256 * 256);
   a.counters = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(a.delta) +
                                            2 * ((rows_pad * sizeof(float) + 255) / 256 * 256));
+  a.ticket = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(a.counters) +
+                                         (rows_pad / 128 * sizeof(unsigned) + 255) / 256 * 256);
   a.deterministic = deterministic;
   a.BH = BH;
   a.N_q = N_q;
@@ -337,13 +371,24 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const 
   a.d = d;
   a.causal = causal;
   a.scale = scale;
-  a.stream = static_cast<cudaStream_t>(stream);
+  a.stream = stream;
   const cudaError_t e = launch_bwd(a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }
   return FA_OK;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+              void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+              int deterministic, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, deterministic, workspace,
+                   workspace_bytes, false, static_cast<cudaStream_t>(stream));
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,

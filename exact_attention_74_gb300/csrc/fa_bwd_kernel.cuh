@@ -11,7 +11,9 @@
 // Three kernels:
 //   prep  -- per query row: D, LSE * log2(e) (both padded to a multiple of 128
 //            rows per head: padding rows get D = 0, LSE = +inf so their P is 0),
-//            and clears the fp32 dQ accumulator.
+//            the per-tile counters and the CTA ticket; in the unordered mode it
+//            also clears the fp32 dQ accumulator (the fixed-order mode's first
+//            partial of each query tile is stored, not added).
 //   main  -- one CTA per (128-key tile, batch*head), K and V resident in shared
 //            memory, looping over the query tiles that can see its keys
 //            (causal: only tiles at or below the diagonal):
@@ -84,6 +86,7 @@ struct Cfg {
 
 struct Params {
   float* dq_acc;
+  unsigned* ticket;      // fixed order: CTAs number themselves in the order they start
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const float* lse2;     // [BH, nq_pad]
@@ -97,13 +100,16 @@ struct Params {
   DevCtl ctl;
 };
 
-// CTA b -> (key tile j, batch*head).  Head-major: the CTAs resident at one
-// time cover only a few heads, so their fp32 dQ accumulators (and Q, dO
-// tiles) stay in L2; within a head, key tile 0 runs first (with a causal
-// mask it sees the most query tiles).  In deterministic mode each query tile
-// takes its partials in decreasing key-tile order, so key tiles run from the
-// last one (a CTA then only waits for CTAs dispatched before it).  Without
-// a mask every query tile takes all key tiles' partials, so a head's CTAs
+// Logical CTA index b -> (key tile j, batch*head).  Head-major: the CTAs
+// resident at one time cover only a few heads, so their fp32 dQ
+// accumulators (and Q, dO tiles) stay in L2; within a head, key tile 0 runs
+// first (with a causal mask it sees the most query tiles).  In the
+// fixed-order mode each query tile takes its partials in decreasing key-tile
+// order, so key tiles run from the last one, and b is a ticket each CTA
+// draws when it starts: every CTA a CTA waits for drew a smaller ticket, so
+// it has already started (and waits for nobody after it), whatever order the
+// hardware dispatches CTAs in and whatever else runs on the GPU.  Without a
+// mask every query tile takes all key tiles' partials, so a head's CTAs
 // running side by side would each wait on the one just ahead: a group of
 // kDetGroup heads is interleaved key tile by key tile, so one wave holds a
 // few consecutive key tiles of each head of the group and most of a CTA's
@@ -133,9 +139,11 @@ template <int D>
 __global__ void __launch_bounds__(256)
 prep_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
             const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
-            float* __restrict__ dq_acc, unsigned* __restrict__ counters, int BH, int N_q, int nq_pad) {
+            float* __restrict__ dq_acc, unsigned* __restrict__ counters, unsigned* __restrict__ ticket,
+            int clear_acc, int BH, int N_q, int nq_pad) {
   constexpr int kPer = D / 32;     // elements per lane
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
   const long long rows = static_cast<long long>(BH) * nq_pad;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows;
@@ -155,13 +163,13 @@ prep_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict
           acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
           acc = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(bw[i] & 0xffff0000u), acc);
         }
-        *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (clear_acc) *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
         const uint32_t a = *reinterpret_cast<const uint32_t*>(O + base);
         const uint32_t b = *reinterpret_cast<const uint32_t*>(dO + base);
         acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
         acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
-        *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
+        if (clear_acc) *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -212,15 +220,14 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   auto bar = [&](int i) -> uint32_t { return sb + C::kBar + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+  int* logical_slot = reinterpret_cast<int*>(smem + C::kMisc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int j, bh;
-  block_tile<DET>(p, static_cast<int>(blockIdx.x), j, bh);
-  const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
-  const int n_it = max(0, p.n_q_tiles - i0);
 
   if (threadIdx.x == 0) {
+    // fixed order: the ticket (its latency overlaps the set-up below)
+    const int b = DET ? static_cast<int>(atomicAdd(p.ticket, 1u)) : static_cast<int>(blockIdx.x);
     mbar_init(bar(C::kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kQFull + s), 1);      // Q tile + LSE and D rows
@@ -238,12 +245,18 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(bar(C::kAccFull), 1);
     *abort_flag = 0;
     mbar_init_fence();
+    *logical_slot = b;
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int logical = *logical_slot;
+  int j, bh;
+  block_tile<DET>(p, logical, j, bh);
+  const int i0 = p.causal ? j : 0;                  // first query tile that sees these keys
+  const int n_it = max(0, p.n_q_tiles - i0);
 
   if (n_it > 0 && warp == 0) {
     // ------------------------------------------------------------ producer
@@ -279,9 +292,11 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           if (!mbar_wait(bar(C::kStagedQ + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
           const int ip = i0 + t - 2;
           unsigned* cnt = p.counters + static_cast<size_t>(bh) * p.n_q_tiles + ip;
+          bool first = false;     // fixed order: the first partial of a query tile is stored
           if constexpr (DET) {
             // key tiles above this one (up to the last that sees query tile ip) add first
             const int top = p.causal ? min(ip, p.n_kv_tiles - 1) : p.n_kv_tiles - 1;
+            first = j == top;
             if (!wait_counter(cnt, static_cast<unsigned>(top - j), p.ctl, abort_flag)) break;
             fence_proxy_async_global();
           }
@@ -291,9 +306,12 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             if (c == 1 && !mbar_wait(bar(C::kStaged + s), ((t - 2) >> 1) & 1, p.ctl, abort_flag)) break;
             if (c < kBoxes)
               for (int hf = 0; hf < 2; ++hf)
-                for (int rk = 0; rk < 4; ++rk)
-                  tma_reduce_add_3d(&tmDQ, sb + C::q_off(s) + c * C::kTile + (hf * 4 + rk) * 4096,
-                                    hf * (D / 2) + 32 * c, ip * kBN + rk * 32, bh);
+                for (int rk = 0; rk < 4; ++rk) {
+                  const uint32_t src = sb + C::q_off(s) + c * C::kTile + (hf * 4 + rk) * 4096;
+                  const int x = hf * (D / 2) + 32 * c, y = ip * kBN + rk * 32;
+                  if (first) tma_store_3d(&tmDQ, src, x, y, bh);
+                  else tma_reduce_add_3d(&tmDQ, src, x, y, bh);
+                }
             bulk_commit_group();
           }
           if (*abort_flag) break;
@@ -302,7 +320,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         if (t == max(0, n_it - 4)) {
           // The CTA that this SM (or another) runs one wave later reads a
           // K/V tile nobody has touched yet: start it towards L2 now.
-          const int nb = static_cast<int>(blockIdx.x) + p.n_sms;
+          const int nb = logical + p.n_sms;
           if (nb < static_cast<int>(gridDim.x)) {
             int nj, nbh;
             block_tile<DET>(p, nb, nj, nbh);
@@ -656,12 +674,13 @@ cudaError_t launch(const BwdLaunch& a) {
     const long long blocks = (rows + 7) / 8;
     prep_kernel<D><<<static_cast<unsigned>(blocks < 65535 * 8 ? blocks : 65535 * 8), 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, lse2, a.delta,
-        a.dq_acc, a.counters, a.BH, a.N_q, nq_pad);
+        a.dq_acc, a.counters, a.ticket, a.deterministic ? 0 : 1, a.BH, a.N_q, nq_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   Params p;
   p.dq_acc = a.dq_acc;
+  p.ticket = a.ticket;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.lse2 = lse2;

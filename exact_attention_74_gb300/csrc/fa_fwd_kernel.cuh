@@ -32,8 +32,14 @@
 // P (as the P V product consumes it): with tau > 0 that largest P (up to
 // 2^tau) is not a power of two, and in near-one-hot rows its rounding would
 // otherwise show in O undamped; the residuals of the other, smaller
-// probabilities average out like any bf16 rounding of P.  Some of the exponentials take the FMA-pipe cubic
-// emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
+// probabilities average out like any bf16 rounding of P.  A query tile whose
+// rows see at most one key tile (the first tile of a causal grid, or
+// N_kv <= 128) has few keys per row, where rounding a couple of comparable
+// probabilities to bf16 (2^-8 relative each) moves O by up to 2^-8 |v|: its
+// P V takes P in two bf16 parts instead, hi = bf16(P) over S columns [0, 64)
+// and lo = bf16(P - hi) over the dead columns [64, 128), as two products, so
+// that P is carried to ~2^-16.  Some of the exponentials take the FMA-pipe
+// cubic emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
 //
 // Causal masking skips every key tile that lies wholly above the diagonal;
 // only the last key tile of each query tile needs an element mask (it holds
@@ -201,12 +207,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (k == D / 16 - 3) peek();
         }
       };
-      auto issue_PV = [&](int t, int vslot, bool acc) {
+      // O_t (+)= P_t V; `split`: P was written in two bf16 parts (see the
+      // header), the low part over S columns [64, 128), added by a second
+      // product.
+      auto issue_PV = [&](int t, int vslot, bool acc, bool split) {
         const uint32_t va = sb + C::kKVOff + vslot * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           mma_ts(tmem + C::col_O(t), tmem + C::col_S(t) + 8 * k,
                  sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, (acc || k > 0) ? 1u : 0u);
+        }
+        if (split) {
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            mma_ts(tmem + C::col_O(t), tmem + C::col_S(t) + 64 + 8 * k,
+                   sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, 1u);
         }
       };
       // K_j and V_j are ring loads 2j and 2j+1, in the producer's order.
@@ -244,7 +259,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           p_ready[t] = false;
           if (!ok) break;
           tc_fence_after();
-          issue_PV(t, iv % C::kSlots, j > 0);
+          issue_PV(t, iv % C::kSlots, j > 0, n_t[t] == 1);
           if (j + 1 < n_t[t]) {
             if (t == 0) {
               issue_S(0, ik % C::kSlots, [&] {
@@ -343,27 +358,47 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-m_ref, -m_ref);
       float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
-      uint32_t pk[64];
+      if (nt > 1) {
+        float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
+        uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
-        const float e0 = ex2_mix<EMU>(x.x, 2 * i);
-        const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
-        sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
-        if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
-        const uint32_t w = pack_bf16x2(e0, e1);
-        pk[i] = w;
+        for (int i = 0; i < 64; ++i) {
+          const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+          const float e0 = ex2_mix<EMU>(x.x, 2 * i);
+          const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
+          sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
+          if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
+          const uint32_t w = pack_bf16x2(e0, e1);
+          pk[i] = w;
+        }
+        {
+          // the block's largest P: with every exponential on the ex2 unit,
+          // recomputed exactly as its element was (same fused multiply-add)
+          const float pm = EMU > 0 ? pmax : ex2_hw(fmaf(mxs, c, -m_ref));
+          const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
+          lr += pmr - pm;
+        }
+        tmem_st_x64(tS, pk);   // waits for its own stores
+      } else {
+        // one key tile per row: P = hi + lo, both bf16 (no residual needed)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int q = 16 * h + i;
+            const float2 x = fma2(make_float2(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])), c2, neg2);
+            const float e0 = ex2_mix<EMU>(x.x, 2 * q);
+            const float e1 = ex2_mix<EMU>(x.y, 2 * q + 1);
+            sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
+            hi[i] = pack_bf16x2(e0, e1);
+            lo[i] = pack_bf16x2(e0 - __uint_as_float(hi[i] << 16), e1 - __uint_as_float(hi[i] & 0xffff0000u));
+          }
+          tmem_st_x16(tS + 16 * h, hi);
+          tmem_st_x16(tS + 64 + 16 * h, lo);
+        }
       }
       l += (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
-      {
-        // the block's largest P: with every exponential on the ex2 unit,
-        // recomputed exactly as its element was (same fused multiply-add)
-        const float pm = EMU > 0 ? pmax : ex2_hw(fmaf(mxs, c, -m_ref));
-        const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
-        lr += pmr - pm;
-      }
-      tmem_st_x64(tS, pk);   // waits for its own stores
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::kPFull + t));

@@ -38,6 +38,7 @@ struct BwdLaunch {
   float* dq_acc;      // workspace: fp32 [B*H, N_q, d]
   float* delta;       // workspace: fp32 [B*H, N_q rounded up to 128], then LSE*log2e, same shape
   unsigned* counters; // workspace: [B*H, N_q / 128 rounded up] dQ contributions applied (deterministic mode)
+  unsigned* ticket;   // workspace: one word, the next CTA ticket (deterministic mode)
   int deterministic;
   int BH, N_q, N_kv, d, causal;
   int n_sms;          // multiprocessor count of the device
@@ -75,6 +76,12 @@ cudaError_t launch_fwd_fp8(const Fp8Launch& a);
 
 // Defined in fa_api.cu.
 int device_ctl(DevCtl* ctl, int* n_sms = nullptr);
+// The backward entry point's checks and launches; internal_workspace = the
+// library's own scratch array (not checked as a caller allocation).
+int bwd_entry(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+              void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+              int deterministic, void* workspace, size_t workspace_bytes, bool internal_workspace,
+              cudaStream_t stream);
 int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows = 128);
 int make_map_f32(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_cols, int box_rows);
 // 3-D map over a contiguous u8 [BH, rows, inner] tensor, 128 x 128 x 1 boxes, 128-byte swizzle.

@@ -28,7 +28,10 @@
  *
  * Errors: every entry point returns an fa_status.  Argument checks happen on
  * the host before anything is launched; a rejected call launches nothing and
- * leaves all buffers untouched.  A launch failure returns FA_ERR_CUDA.  Every
+ * leaves all buffers untouched.  Besides sizes and alignment they include the
+ * memory behind every tensor and workspace pointer: it must be device memory
+ * the current device can address (cudaMalloc, a memory pool, managed memory);
+ * host memory, pinned or not, is refused with FA_ERR_INVALID.  A launch failure returns FA_ERR_CUDA.  Every
  * wait inside the kernels is bounded in time; a wait that runs out sets a
  * device status word that fa_get_last_device_status() reports as
  * FA_ERR_TIMEOUT (the outputs of that call are then undefined).  Nothing
@@ -46,7 +49,7 @@ extern "C" {
 
 typedef enum {
   FA_OK = 0,
-  FA_ERR_INVALID = 1,      /* null pointer, size < 1, causal not 0/1, bad scale */
+  FA_ERR_INVALID = 1,      /* null or non-device pointer, size < 1, causal not 0/1, bad scale */
   FA_ERR_UNSUPPORTED = 2,  /* head dimension d not supported by the call; no sm_103 device */
   FA_ERR_ALIGN = 3,        /* a pointer not 16-byte aligned (TMA requirement) */
   FA_ERR_WORKSPACE = 4,    /* fa_bwd workspace null or smaller than required */
@@ -132,8 +135,9 @@ int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * for this problem: an fp32 dQ accumulator [B, H, N_q, d], then two fp32 row
  * vectors D = rowsum(dO * O) and LSE * log2(e), each [B, H, N_q rounded up
  * to a multiple of 128], then one 32-bit counter per 128-row query tile
- * [B, H, ceil(N_q / 128)]; every part is rounded up to 256 bytes.  Returns 0
- * for invalid sizes and for d = 256 (no backward).
+ * [B, H, ceil(N_q / 128)], then one 32-bit ticket counter; every part is
+ * rounded up to 256 bytes.  Returns 0 for invalid sizes and for d = 256 (no
+ * backward).
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N_q, int N_kv, int d);
 
@@ -163,7 +167,10 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O,
  *                    the same inputs give bit-identical dQ, dK and dV
  *                    ("論文解説: FlashAttention-4 ...", 実験結果: the
  *                    deterministic backward mode).  Key tiles then wait for
- *                    one another through the workspace counters.
+ *                    one another through the workspace counters; the work
+ *                    items are numbered in the order their thread blocks
+ *                    start, so a block only ever waits for blocks that are
+ *                    already running, whatever else runs on the device.
  * Other arguments, the workspace and the errors are those of fa_bwd;
  * deterministic outside {0, 1} returns FA_ERR_INVALID.
  */
@@ -192,9 +199,11 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O,
  *     (at d = 128 that is about 32,000 query rows B*H*N_q; use fa_bwd with a
  *     workspace of your own beyond that).  Other argument errors are those
  *     of fa_bwd.
- *   - The first call on a device looks up the scratch's device address with
- *     that device current (a CUDA runtime query, no allocation); make that
- *     first call before any stream capture on that device.
+ *   - Every call looks up the scratch's device address on the current
+ *     device (a CUDA runtime query, no allocation), so the address stays
+ *     right if the device's context is reset.  The first call on a device may
+ *     load the library's device code there; make that first call before any
+ *     stream capture on that device.
  *   - Every call on a device shares the one scratch area.  Each call clears
  *     what it needs before using it, but calls that can overlap on the GPU
  *     (for example on two streams without ordering between them) race on it

@@ -115,10 +115,11 @@ def test_lse_needs_only_4_byte_alignment(lib):
 
 def test_workspace_bytes(lib):
     # fp32 dQ accumulator + two fp32 row vectors padded to 128 rows + one counter per
-    # 128-row tile, each part rounded up to 256 B
-    assert fa.fa_bwd_workspace_bytes(2, 16, 8192, 8192, 128) == 2 * 16 * 8192 * (128 * 4 + 2 * 4) + 2 * 16 * 64 * 4
-    assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 64) == 768 + 2 * 512 + 256
-    assert fa.fa_bwd_workspace_bytes(3, 1, 130, 5, 128) == 3 * 130 * 128 * 4 + 2 * 3 * 256 * 4 + 256
+    # 128-row tile + the ticket word, each part rounded up to 256 B
+    assert fa.fa_bwd_workspace_bytes(2, 16, 8192, 8192, 128) == \
+        2 * 16 * 8192 * (128 * 4 + 2 * 4) + 2 * 16 * 64 * 4 + 256
+    assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 64) == 768 + 2 * 512 + 256 + 256
+    assert fa.fa_bwd_workspace_bytes(3, 1, 130, 5, 128) == 3 * 130 * 128 * 4 + 2 * 3 * 256 * 4 + 256 + 256
     assert fa.fa_bwd_workspace_bytes(1, 1, 0, 5, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 80) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 3, 5, 256) == 0     # forward only at d = 256

@@ -29,7 +29,7 @@ def torch():
     return torch
 
 
-def run_fwd_bwd(torch, w, qb, kb, vb, dob):
+def run_fwd_bwd(torch, w, qb, kb, vb, dob, fwd_out=None):
     B, H, N_q, d = qb.shape
     N_kv = kb.shape[2]
     q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
@@ -38,6 +38,8 @@ def run_fwd_bwd(torch, w, qb, kb, vb, dob):
     st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                    B, H, N_q, N_kv, d, int(w.causal), w.scale, 0)
     assert st == fa.FA_OK
+    if fwd_out is not None:
+        fwd_out.extend([gu.to_f64(o), lse.cpu().numpy().astype(np.float64)])
     dq = gu.Guarded((B, H, N_q, d), torch.bfloat16)
     dk = gu.Guarded((B, H, N_kv, d), torch.bfloat16)
     dv = gu.Guarded((B, H, N_kv, d), torch.bfloat16)
@@ -161,11 +163,28 @@ def _conditioning(q, k, v, o, do, lse, scale):
 
 
 def test_full_size_backward(torch):
+    """The backward workload B2 H16 N8192 d128 causal at full size: its
+    forward (O, LSE) on sampled rows of all 32 heads under the stated bounds
+    and the per-element arithmetic bound, then dQ, dK, dV of 8 whole heads
+    (both batches, first and last heads among them) against the oracle's exact
+    gradients."""
     w = fa_inputs.WORKLOADS["bwd_8k"]
     qb, kb, vb = fa_inputs.make_qkv(w)
     dob = fa_inputs.make_dout(w)
-    dq, dk, dv = run_fwd_bwd(torch, w, qb, kb, vb, dob)
-    for b, h in ((0, 0), (1, 13)):
+    fwd_out = []
+    dq, dk, dv = run_fwd_bwd(torch, w, qb, kb, vb, dob, fwd_out)
+    o, lse = fwd_out
+    rng = np.random.default_rng(w.seed + 99)
+    got, ref, got_l, ref_l, sps = [], [], [], [], []
+    for b in range(w.B):
+        for h in range(w.H):
+            rows = gu.sample_rows(w.N_q, 32, rng)
+            o_ref, lse_ref, sp = gu.oracle_rows(qb, kb, vb, b, h, rows, True, w.scale, with_spread=True)
+            got.append(o[b, h][rows]); ref.append(o_ref); sps.append(sp)
+            got_l.append(lse[b, h][rows]); ref_l.append(lse_ref)
+    gu.assert_o_lse(np.concatenate(got), np.concatenate(got_l), np.concatenate(ref), np.concatenate(ref_l),
+                    f"{w.name} forward (32 heads x 40 rows)", spread_=np.concatenate(sps))
+    for b, h in ((0, 0), (0, 5), (0, 10), (0, 15), (1, 0), (1, 6), (1, 13), (1, 15)):
         q, k, v, do = (fa_inputs.bf16_bits_to_f64(x[b, h]) for x in (qb, kb, vb, dob))
         ref = oracle.head_backward(q, k, v, do, causal=w.causal, scale=w.scale)
         check_grads((dq[b, h], dk[b, h], dv[b, h]), ref, f"{w.name} b{b} h{h}")
@@ -269,6 +288,46 @@ def test_deterministic_full_size_causal(torch):
     b = _bwd_ex(torch, w, t, 1)
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
-    q64, k64, v64, do64 = (fa_inputs.bf16_bits_to_f64(x[1, 5]) for x in (qb, kb, vb, dob))
-    ref = oracle.head_backward(q64, k64, v64, do64, causal=True, scale=w.scale)
-    check_grads([gu.to_f64(x)[1, 5] for x in a], ref, "deterministic bwd_8k b1 h5")
+    got = [gu.to_f64(x) for x in a]
+    for bi, hi in ((0, 0), (0, 11), (1, 5), (1, 15)):
+        q64, k64, v64, do64 = (fa_inputs.bf16_bits_to_f64(x[bi, hi]) for x in (qb, kb, vb, dob))
+        ref = oracle.head_backward(q64, k64, v64, do64, causal=True, scale=w.scale)
+        check_grads([g[bi, hi] for g in got], ref, f"deterministic bwd_8k b{bi} h{hi}")
+
+
+def test_deterministic_beside_a_concurrent_kernel(torch):
+    """The fixed-order backward while another stream keeps SMs busy with long
+    forward launches of this library: its thread blocks then start in an
+    order the hardware picks around the other kernel's.  Every wait must
+    still end (FA_OK), and the gradients must equal, bit for bit, those of a
+    call with the GPU to itself."""
+    w = _wl(2, 8, 2048, 2048, 128, False, seed=123)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    q, k, v, do = (gu.dev_bf16(x) for x in (qb, kb, vb, dob))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N_q), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     w.B, w.H, w.N_q, w.N_kv, w.d, 0, w.scale, 0) == fa.FA_OK
+    solo = _bwd_ex(torch, w, (q, k, v, o, do, lse), 1)
+    # the other kernel: forward launches on 2 x 16 heads of 8192 rows (~1 ms each)
+    bq = torch.randn((2, 16, 8192, 128), device="cuda").to(torch.bfloat16)
+    bo = torch.empty_like(bq)
+    bl = torch.empty((2, 16, 8192), dtype=torch.float32, device="cuda")
+    need = fa.fa_bwd_workspace_bytes(w.B, w.H, w.N_q, w.N_kv, w.d)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    s_other, s_bwd = torch.cuda.Stream(), torch.cuda.Stream()
+    for rep in range(3):
+        dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+        for _ in range(4):
+            assert fa.fa_fwd(bq.data_ptr(), bq.data_ptr(), bq.data_ptr(), bo.data_ptr(), bl.data_ptr(),
+                             2, 16, 8192, 8192, 128, 0, 0.088, s_other.cuda_stream) == fa.FA_OK
+        st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N_q, w.N_kv, w.d, 0,
+                          w.scale, 1, ws.data_ptr(), need, s_bwd.cuda_stream)
+        assert st == fa.FA_OK
+        torch.cuda.synchronize()
+        assert fa.fa_get_last_device_status(0) == fa.FA_OK, f"rep {rep}: a wait ran out"
+        for x, y in zip((dq, dk, dv), solo):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16)), f"rep {rep}"

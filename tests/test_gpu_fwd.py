@@ -2,10 +2,15 @@
 
 Small and ragged problems are compared element by element over the whole
 output; the full-size workloads run at their real sizes (the launch the bench
-times) and are compared on sampled (batch, head, row) outputs that the oracle
-computes one row at a time.  Every call also checks that nothing outside O
-and LSE was written (guard bands), that every output element was written
-(outputs start as NaN), and that no in-kernel wait ran out.
+times): the bench workload B4 H16 N4096 d128 on every element of every head,
+the sequence sweep, the stress workload and the 16k-token d = 256 workload on
+sampled rows of every head, which the oracle computes one row at a time.
+The stated bounds (O max-abs 1e-2, relative RMS 5e-3, LSE max-abs 1e-3)
+apply as written wherever the head dimension is 64 or 128; on top of them
+each element must meet the arithmetic bound of ``gpu_util`` wherever the
+oracle computes it.  Every call also checks that nothing outside O and LSE
+was written (guard bands), that every output element was written (outputs
+start as NaN), and that no in-kernel wait ran out.
 """
 import math
 
@@ -47,12 +52,28 @@ def run_fwd(torch, qb, kb, vb, causal, scale, tau=None, emu=None):
     return gu.to_f64(o.view), lse.view.cpu().numpy().astype(np.float64)
 
 
-def full_compare(torch, w, **kw):
+def relaxed(w):
+    """The extra workloads whose exact outputs leave bf16's reach of 1e-2:
+    head dimension 256 (|O| up to 4.7 on the stress inputs) and the outlier
+    inputs (|O| up to tens)."""
+    return w.d == 256 or w.kind == "outlier"
+
+
+def full_compare(torch, w, with_spread=True, **kw):
     qb, kb, vb = fa_inputs.make_qkv(w)
     o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale, **kw)
     q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
     o_ref, lse_ref = oracle.attention_forward(q, k, v, causal=w.causal, scale=w.scale)
-    return gu.assert_o_lse(o, lse, o_ref, lse_ref, w.name)
+    sp = None
+    if with_spread:
+        sp = np.empty_like(o_ref)
+        for b in range(w.B):
+            for h in range(w.H):
+                sp[b, h] = gu.spread(q[b, h], k[b, h], v[b, h], o_ref[b, h], w.causal, w.scale)
+    if relaxed(w):
+        return gu.assert_o_lse_bf16(o, lse, o_ref, lse_ref, sp, w.name,
+                                    lse_rel=1e-6 if w.kind == "outlier" else 0.0)
+    return gu.assert_o_lse(o, lse, o_ref, lse_ref, w.name, spread_=sp)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -99,29 +120,21 @@ def test_rescale_threshold_on_stress_inputs(torch, tau, emu, d):
 def test_outlier_distribution_accuracy(torch, causal):
     """N(0,1) + N(0,100)*Bernoulli(0.001) inputs (the FlashAttention-3 notes' error study).
 
-    |O| reaches tens here, where one bf16 step is 0.125, so the absolute 1e-2
-    bound of the iid workloads cannot apply; each element must instead lie
-    within one bf16 step (2^-7 relative) of the exact value, the whole tensor
-    within 5e-3 relative RMS, and the LSE within 1e-3 (+1e-6 relative).
+    |O| reaches tens here, where half a bf16 step is 0.06, so the absolute
+    1e-2 bound of the iid workloads cannot apply; each element must instead
+    lie within half a bf16 step of its exact value's binade plus the
+    arithmetic budget (or 1e-2), the whole tensor within 5e-3 relative RMS,
+    and the LSE within 1e-3 (+1e-6 relative).
     """
     w = _wl(1, 4, 1024, 1024, 128, causal, seed=31, kind="outlier")
-    qb, kb, vb = fa_inputs.make_qkv(w)
-    o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale)
-    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
-    o_ref, lse_ref = oracle.attention_forward(q, k, v, causal=w.causal, scale=w.scale)
-    err = np.abs(o - o_ref)
-    assert np.all(err <= np.maximum(gu.O_MAX_ABS, 2.0 ** -7 * np.abs(o_ref)))
-    assert gu.rel_rms(o, o_ref) <= gu.O_REL_RMS
-    assert np.all(np.abs(lse - lse_ref) <= gu.LSE_MAX_ABS + 1e-6 * np.abs(lse_ref))
-    rmse = float(np.sqrt(np.mean((o - o_ref) ** 2)))
-    print(f"outlier inputs causal={causal}: O RMSE vs fp64 {rmse:.3e}")
+    full_compare(torch, w)
 
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_heads(torch, causal):
     """B*H = 80,000 heads of 5 query rows and 7 keys, more than the 65,535 a
     grid's y or z extent allows: every head is computed and compared."""
-    full_compare(torch, _wl(2, 40000, 5, 7, 64, causal, seed=41))
+    full_compare(torch, _wl(2, 40000, 5, 7, 64, causal, seed=41), with_spread=False)
 
 
 def test_accuracy_report_outliers_4k(torch, capsys):
@@ -150,33 +163,59 @@ def test_accuracy_report_outliers_4k(torch, capsys):
     assert rmse <= 2.0 * floor
 
 
-def sampled_compare(torch, w, heads, nrows, **kw):
+def sampled_compare(torch, w, nrows, heads=None, **kw):
+    """Run the workload at full size, then compare sampled rows of the given
+    (batch, head) pairs (default: every head) with the oracle, one row at a
+    time, each row with its per-element arithmetic bound."""
     qb, kb, vb = fa_inputs.make_qkv(w)
     o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale, **kw)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
     rng = np.random.default_rng(w.seed + 99)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)] if heads is None else heads
+    got, ref, ref_l, got_l, sps = [], [], [], [], []
     for b, h in heads:
         rows = gu.sample_rows(w.N_q, nrows, rng)
-        o_ref, lse_ref = gu.oracle_rows(qb, kb, vb, b, h, rows, w.causal, w.scale)
-        gu.assert_o_lse(o[b, h][rows], lse[b, h][rows], o_ref, lse_ref, f"{w.name} b{b} h{h}")
+        o_ref, lse_ref, sp = gu.oracle_rows(qb, kb, vb, b, h, rows, w.causal, w.scale, with_spread=True)
+        got.append(o[b, h][rows]); ref.append(o_ref); sps.append(sp)
+        got_l.append(lse[b, h][rows]); ref_l.append(lse_ref)
+    got, ref, sps = np.concatenate(got), np.concatenate(ref), np.concatenate(sps)
+    got_l, ref_l = np.concatenate(got_l), np.concatenate(ref_l)
+    what = f"{w.name} ({len(heads)} heads x {nrows}+ rows)"
+    if relaxed(w):
+        return gu.assert_o_lse_bf16(got, got_l, ref, ref_l, sps, what)
+    return gu.assert_o_lse(got, got_l, ref, ref_l, what, spread_=sps)
 
 
 @pytest.mark.parametrize("name", ["fwd_4k", "fwd_4k_causal"])
 def test_full_size_4k(torch, name):
+    """The bench workload B4 H16 N4096 d128: every element of all 64 heads
+    against the oracle under the stated bounds, then the per-element
+    arithmetic bound on sampled rows of every head."""
     w = fa_inputs.WORKLOADS[name]
-    sampled_compare(torch, w, [(0, 0), (1, 7), (3, 15)], 96)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    o, lse = run_fwd(torch, qb, kb, vb, w.causal, w.scale)
+    q, k, v = (fa_inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    o_ref, lse_ref = oracle.attention_forward(q, k, v, causal=w.causal, scale=w.scale)
+    gu.assert_o_lse(o, lse, o_ref, lse_ref, f"{name} all {w.B * w.H} heads")
+    rng = np.random.default_rng(w.seed + 99)
+    for b in range(w.B):
+        for h in range(w.H):
+            rows = gu.sample_rows(w.N_q, 24, rng)
+            sp = gu.spread(q[b, h][rows], k[b, h], v[b, h], o_ref[b, h][rows], w.causal, w.scale, rows=rows)
+            err = np.abs(o[b, h][rows] - o_ref[b, h][rows])
+            gu._assert_element_bound(err, o_ref[b, h][rows], sp, f"{name} b{b} h{h}")
 
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("idx", range(6))
 def test_sequence_sweep(torch, causal, idx):
     w = fa_inputs.sweep_workloads(causal)[idx]
-    sampled_compare(torch, w, [(0, 0), (w.B - 1, 15)], 48)
+    sampled_compare(torch, w, 40 if w.N_q <= 8192 else 24)
 
 
 def test_stress_full_size(torch):
     w = fa_inputs.WORKLOADS["stress_8k"]
-    sampled_compare(torch, w, [(0, 0), (1, 9)], 64)
+    sampled_compare(torch, w, 48)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -184,4 +223,4 @@ def test_full_size_hdim256(torch, causal):
     """B2 H16 N8192 d256: 16k tokens at the largest head dimension of the
     FlashAttention-3 sweep, the launch the bench times."""
     w = fa_inputs.Workload("hdim256_8k", 2, 16, 8192, 8192, 256, causal, 1.0 / 16.0, 20267)
-    sampled_compare(torch, w, [(0, 0), (1, 15)], 48)
+    sampled_compare(torch, w, 24)
