@@ -2,7 +2,8 @@
 
 A step is one pass of the whole path over one batch of synthetic input:
 fa_fwd, then fa_bwd on the forward's O and LSE (the backward's kernels:
-D = rowsum(dO*O), then the main pass).  The step's workload is B=4, H=16,
+D = rowsum(dO*O), the main pass, the dQ conversion).  The step's
+workload is B=4, H=16,
 N=4096, d=128, bf16, non-causal, with inputs larger than L2 (Q, K, V, O, dO:
 5 x 67 MB).
 
@@ -432,7 +433,7 @@ def run_gpu(args):
                     "ms_per_launch": main_ms, "time_source": time_source,
                     "peak_source": f"{peaks['source']} (burst bf16 GEMM)",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "call": {"what": "fa_bwd (every kernel of the backward call), CUDA events in the timed region",
+                    "call": {"what": "fa_bwd (prep + main + convert), CUDA events in the timed region",
                              "achieved": w.bwd_flops() / (med_bwd * 1e-3) / 1e12,
                              "frac": w.bwd_flops() / (med_bwd * 1e-3) / 1e12 / peak,
                              "traffic": ncu_traffic("fa_bwd")}}

@@ -40,7 +40,8 @@
 //                        layout, handed to the producer, which adds it into
 //                        the fp32 accumulator with TMA reduce-adds
 //            dK and dV stay in tensor memory for the whole loop and are
-//            written once at the end.
+//            written once at the end.  CTAs number themselves with a ticket
+//            when they start and take their (key tile, head) from it.
 //   convert -- dQ = bf16(scale * accumulator).
 // Tensor-memory columns: S^T [0,128), over which P^T [0,64) and dS^T
 // [64,128) land as bf16 pairs (the A operands of dV and dK); dP^T and then
@@ -86,7 +87,7 @@ struct Cfg {
 
 struct Params {
   float* dq_acc;
-  unsigned* ticket;      // fixed order: CTAs number themselves in the order they start
+  unsigned* ticket;      // CTAs number themselves in the order they start
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const float* lse2;     // [BH, nq_pad]
@@ -141,45 +142,63 @@ prep_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict
             const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
             float* __restrict__ dq_acc, unsigned* __restrict__ counters, unsigned* __restrict__ ticket,
             int clear_acc, int BH, int N_q, int nq_pad) {
-  constexpr int kPer = D / 32;     // elements per lane
+  // A row of O (and of dO) is D bf16 = L 16-byte pieces, one per lane; a warp
+  // takes 32 / L rows at a time and keeps kU such groups of loads in flight.
+  constexpr int L = D / 8;
+  constexpr int kRows = 32 / L;
+  constexpr int kU = 4;
   const int lane = threadIdx.x & 31;
+  const int sub = lane / L;               // row of the group
+  const int li = lane % L;                // 16-byte piece of the row
   if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
   const long long rows = static_cast<long long>(BH) * nq_pad;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows;
-       r += warps) {
-    const int bh = static_cast<int>(r / nq_pad);
-    const int q = static_cast<int>(r % nq_pad);
-    if ((q & 127) == 0 && lane == 0) counters[r >> 7] = 0u;   // one per 128-row query tile
-    if (q < N_q) {
-      const size_t base = (static_cast<size_t>(bh) * N_q + q) * D + lane * kPer;
+  const long long wpb = blockDim.x / 32;
+  const long long step = static_cast<long long>(gridDim.x) * wpb * kRows * kU;
+  for (long long r0 = (static_cast<long long>(blockIdx.x) * wpb + threadIdx.x / 32) * kRows * kU; r0 < rows;
+       r0 += step) {
+    uint4 a[kU], b[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long r = r0 + u * kRows + sub;
+      const int bh = static_cast<int>(r / nq_pad);
+      const int q = static_cast<int>(r % nq_pad);
+      a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows && q < N_q) {
+        const size_t off = (static_cast<size_t>(bh) * N_q + q) * D + li * 8;
+        a[u] = *reinterpret_cast<const uint4*>(O + off);
+        b[u] = *reinterpret_cast<const uint4*>(dO + off);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long r = r0 + u * kRows + sub;
+      const int bh = static_cast<int>(r / nq_pad);
+      const int q = static_cast<int>(r % nq_pad);
+      const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
       float acc = 0.f;
-      if constexpr (kPer == 4) {
-        const uint2 a = *reinterpret_cast<const uint2*>(O + base);
-        const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
-        const uint32_t aw[2] = {a.x, a.y}, bw[2] = {b.x, b.y};
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
-          acc = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(bw[i] & 0xffff0000u), acc);
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(bw[e] & 0xffff0000u), acc);
+      }
+#pragma unroll
+      for (int o = L / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (r >= rows) continue;
+      if (li == 0) {
+        if ((q & 127) == 0) counters[r >> 7] = 0u;   // one per 128-row query tile
+        if (q < N_q) {
+          delta[r] = acc;
+          lse2[r] = lse[static_cast<size_t>(bh) * N_q + q] * 1.4426950408889634f;
+        } else {
+          delta[r] = 0.f;
+          lse2[r] = INFINITY;
         }
-        if (clear_acc) *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(O + base);
-        const uint32_t b = *reinterpret_cast<const uint32_t*>(dO + base);
-        acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
-        acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
-        if (clear_acc) *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
       }
+      if (clear_acc && q < N_q) {
+        float4* row = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * N_q + q) * D);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) {
-        delta[r] = acc;
-        lse2[r] = lse[static_cast<size_t>(bh) * N_q + q] * 1.4426950408889634f;
+        for (int k = 0; k < D / 4 / L; ++k) row[li + k * L] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    } else if (lane == 0) {
-      delta[r] = 0.f;
-      lse2[r] = INFINITY;
     }
   }
 }
@@ -226,8 +245,8 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    // fixed order: the ticket (its latency overlaps the set-up below)
-    const int b = DET ? static_cast<int>(atomicAdd(p.ticket, 1u)) : static_cast<int>(blockIdx.x);
+    // the ticket (its latency overlaps the set-up below)
+    const int b = static_cast<int>(atomicAdd(p.ticket, 1u));
     mbar_init(bar(C::kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kQFull + s), 1);      // Q tile + LSE and D rows
@@ -671,7 +690,7 @@ cudaError_t launch(const BwdLaunch& a) {
   float* lse2 = a.delta + static_cast<size_t>(a.BH) * nq_pad;
   {
     const long long rows = static_cast<long long>(a.BH) * nq_pad;
-    const long long blocks = (rows + 7) / 8;
+    const long long blocks = (rows + 8 * 4 * (256 / D) - 1) / (8 * 4 * (256 / D));   // rows per block: 8 warps x 4 groups
     prep_kernel<D><<<static_cast<unsigned>(blocks < 65535 * 8 ? blocks : 65535 * 8), 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, lse2, a.delta,
         a.dq_acc, a.counters, a.ticket, a.deterministic ? 0 : 1, a.BH, a.N_q, nq_pad);

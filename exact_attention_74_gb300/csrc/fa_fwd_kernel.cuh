@@ -35,11 +35,12 @@
 // probabilities average out like any bf16 rounding of P.  A query tile whose
 // rows see at most one key tile (the first tile of a causal grid, or
 // N_kv <= 128) has few keys per row, where rounding a couple of comparable
-// probabilities to bf16 (2^-8 relative each) moves O by up to 2^-8 |v|: its
-// P V takes P in two bf16 parts instead, hi = bf16(P) over S columns [0, 64)
-// and lo = bf16(P - hi) over the dead columns [64, 128), as two products, so
-// that P is carried to ~2^-16.  Some of the exponentials take the FMA-pipe
-// cubic emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
+// probabilities to bf16 (2^-8 relative each) moves O by up to 2^-8 |v|: that
+// tile's single step writes P in two bf16 parts instead, hi = bf16(P) over S
+// columns [0, 64) and lo = bf16(P - hi) over the dead columns [64, 128), and
+// P V is two products, so that P is carried to ~2^-16 (this path is kept out
+// of the main loop).  Some of the exponentials take the FMA-pipe cubic
+// emulation (ソフトウェア指数関数エミュレーション) instead of MUFU.
 //
 // Causal masking skips every key tile that lies wholly above the diagonal;
 // only the last key tile of each query tile needs an element mask (it holds
@@ -48,6 +49,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "exp2.cuh"
 #include "fa_internal.h"
@@ -108,7 +111,10 @@ __device__ __forceinline__ float ex2_mix(float x, int col) {
   return ex2_hw(x);
 }
 
-template <int D, int EMU>
+// SPLIT: the grid may hold query tiles whose rows see one key tile (causal,
+// or N_kv <= 128), which take the two-part P path; grids without such tiles
+// run an instance that carries none of its code.
+template <int D, int EMU, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -207,22 +213,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (k == D / 16 - 3) peek();
         }
       };
-      // O_t (+)= P_t V; `split`: P was written in two bf16 parts (see the
-      // header), the low part over S columns [64, 128), added by a second
-      // product.
-      auto issue_PV = [&](int t, int vslot, bool acc, bool split) {
+      auto issue_PV = [&](int t, int vslot, bool acc) {
         const uint32_t va = sb + C::kKVOff + vslot * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           mma_ts(tmem + C::col_O(t), tmem + C::col_S(t) + 8 * k,
                  sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, (acc || k > 0) ? 1u : 0u);
         }
-        if (split) {
+      };
+      // O_t += P_lo V for a tile whose P was written in two bf16 parts (its
+      // only key step): the low part lies over S columns [64, 128).
+      auto issue_PV_lo = [&](int t, int vslot) {
+        const uint32_t va = sb + C::kKVOff + vslot * C::kTileBytes;
 #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            mma_ts(tmem + C::col_O(t), tmem + C::col_S(t) + 64 + 8 * k,
-                   sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, 1u);
-        }
+        for (int k = 0; k < kBN / 16; ++k)
+          mma_ts(tmem + C::col_O(t), tmem + C::col_S(t) + 64 + 8 * k,
+                 sdesc_sw128(va + k * 2048, kPanelBytes, 1024), idO, 1u);
       };
       // K_j and V_j are ring loads 2j and 2j+1, in the producer's order.
       // Their slots are released by the softmax warps (see there), so the
@@ -243,13 +249,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       }
       uint32_t pph[2] = {0, 0};
       bool kv_ready = false, p_ready[2] = {false, false};
-      for (int j = 0; j < n_max && ok; ++j) {
+      // One key step of both tiles.  `first` (a compile-time tag) marks the
+      // first step, the only one where a tile may take its P in two parts:
+      // the per-step loop itself carries no test for it.
+      auto step = [&](const int j, auto first) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;       // V_j, K_{j+1}
         const bool has_next = j + 1 < n_max;
         if (!kv_ready) {
           ok = mbar_wait(bar(kv_bar(iv)), kv_par(iv), p.ctl, abort_flag);
           if (ok && has_next) ok = mbar_wait(bar(kv_bar(ik)), kv_par(ik), p.ctl, abort_flag);
-          if (!ok) break;
+          if (!ok) return;
         }
         kv_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
@@ -259,7 +268,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           p_ready[t] = false;
           if (!ok) break;
           tc_fence_after();
-          issue_PV(t, iv % C::kSlots, j > 0, n_t[t] == 1);
+          issue_PV(t, iv % C::kSlots, j > 0);
+          if constexpr (decltype(first)::value)
+            if (SPLIT && n_t[t] == 1) issue_PV_lo(t, iv % C::kSlots);
           if (j + 1 < n_t[t]) {
             if (t == 0) {
               issue_S(0, ik % C::kSlots, [&] {
@@ -280,7 +291,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tc_commit(bar(C::kOFull + t));
           }
         }
-      }
+      };
+      if (n_max > 0 && ok) step(0, std::true_type{});
+      for (int j = 1; j < n_max && ok; ++j) step(j, std::false_type{});
     }
   } else {
     // -------------------------------------------------------------- softmax
@@ -298,7 +311,54 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     float l = 0.f;      // sum of the fp32 probabilities: gives the LSE
     float lr = 0.f;     // rounding residuals of the blocks' largest P (see the header)
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
+    if (SPLIT && nt == 1) {
+      // ---- the tile's only key step, P in two bf16 parts (see the header)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), 0, p.ctl, abort_flag));
+      if (ok) {
+        if (releaser && r_in_tile == 0) mbar_arrive(bar(C::kKVEmpty + 0));
+        tc_fence_after();
+        uint32_t s[128];
+        tmem_ld_x128(tS, s);
+        int lim = p.N_kv - 1;
+        if (p.causal) lim = min(lim, row);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > lim) s[i] = __float_as_uint(-INFINITY);
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 128; i += 8) {
+          mx[0] = max3(mx[0], __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+          mx[1] = max3(mx[1], __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+          mx[2] = max3(mx[2], __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
+          mx[3] = max3(mx[3], __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+        }
+        m_ref = c * fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
+        const float2 c2 = make_float2(c, c);
+        const float2 neg2 = make_float2(-m_ref, -m_ref);
+        float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int q = 16 * h + i;
+            const float2 x = fma2(make_float2(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])), c2, neg2);
+            const float e0 = ex2_mix<EMU>(x.x, 2 * q);
+            const float e1 = ex2_mix<EMU>(x.y, 2 * q + 1);
+            sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
+            hi[i] = pack_bf16x2(e0, e1);
+            lo[i] = pack_bf16x2(e0 - __uint_as_float(hi[i] << 16), e1 - __uint_as_float(hi[i] & 0xffff0000u));
+          }
+          tmem_st_x16(tS + 16 * h, hi);
+          tmem_st_x16(tS + 64 + 16 * h, lo);
+        }
+        l = (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kPFull + t));
+      }
+    }
+    for (int j = 0; j < nt && !(SPLIT && nt == 1); ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), j & 1, p.ctl, abort_flag));
       if (!ok) break;
       // S_t,j complete means every product queued before it is complete too:
@@ -358,47 +418,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-m_ref, -m_ref);
       float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (nt > 1) {
-        float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
-        uint32_t pk[64];
+      float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
+      uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
-          const float e0 = ex2_mix<EMU>(x.x, 2 * i);
-          const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
-          sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
-          if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
-          const uint32_t w = pack_bf16x2(e0, e1);
-          pk[i] = w;
-        }
-        {
-          // the block's largest P: with every exponential on the ex2 unit,
-          // recomputed exactly as its element was (same fused multiply-add)
-          const float pm = EMU > 0 ? pmax : ex2_hw(fmaf(mxs, c, -m_ref));
-          const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
-          lr += pmr - pm;
-        }
-        tmem_st_x64(tS, pk);   // waits for its own stores
-      } else {
-        // one key tile per row: P = hi + lo, both bf16 (no residual needed)
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int q = 16 * h + i;
-            const float2 x = fma2(make_float2(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])), c2, neg2);
-            const float e0 = ex2_mix<EMU>(x.x, 2 * q);
-            const float e1 = ex2_mix<EMU>(x.y, 2 * q + 1);
-            sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
-            hi[i] = pack_bf16x2(e0, e1);
-            lo[i] = pack_bf16x2(e0 - __uint_as_float(hi[i] << 16), e1 - __uint_as_float(hi[i] & 0xffff0000u));
-          }
-          tmem_st_x16(tS + 16 * h, hi);
-          tmem_st_x16(tS + 64 + 16 * h, lo);
-        }
+      for (int i = 0; i < 64; ++i) {
+        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+        const float e0 = ex2_mix<EMU>(x.x, 2 * i);
+        const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
+        sum[i & 1] = add2(sum[i & 1], make_float2(e0, e1));
+        if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
+        const uint32_t w = pack_bf16x2(e0, e1);
+        pk[i] = w;
       }
       l += (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
+      {
+        // the block's largest P: with every exponential on the ex2 unit,
+        // recomputed exactly as its element was (same fused multiply-add)
+        const float pm = EMU > 0 ? pmax : ex2_hw(fmaf(mxs, c, -m_ref));
+        const float pmr = __uint_as_float(pack_bf16x2(pm, pm) << 16);   // as rounded for P V
+        lr += pmr - pm;
+      }
+      tmem_st_x64(tS, pk);   // waits for its own stores
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::kPFull + t));
@@ -437,7 +477,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   }
 }
 
-template <int D, int EMU>
+template <int D, int EMU, bool SPLIT>
 cudaError_t launch(const FwdLaunch& a) {
   using C = Cfg<D>;
   Params p;
@@ -452,7 +492,7 @@ cudaError_t launch(const FwdLaunch& a) {
   p.c = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.tau = a.tau;
   p.ctl = a.ctl;
-  auto kern = fwd_kernel<D, EMU>;
+  auto kern = fwd_kernel<D, EMU, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_qpairs) * p.BH;
@@ -461,14 +501,22 @@ cudaError_t launch(const FwdLaunch& a) {
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_any(const FwdLaunch& a) {
+template <int D, bool SPLIT>
+cudaError_t launch_emu(const FwdLaunch& a) {
   switch (a.emu_per_32) {
-    case 0: return launch<D, 0>(a);
-    case 8: return launch<D, 8>(a);
-    case 16: return launch<D, 16>(a);
+    case 0: return launch<D, 0, SPLIT>(a);
+    case 8: return launch<D, 8, SPLIT>(a);
+    case 16: return launch<D, 16, SPLIT>(a);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int D>
+cudaError_t launch_any(const FwdLaunch& a) {
+  // a query tile sees a single key tile only with a causal mask (the first
+  // one) or when all keys fit in one tile
+  const bool split = a.causal || a.N_kv <= kBN;
+  return split ? launch_emu<D, true>(a) : launch_emu<D, false>(a);
 }
 
 }  // namespace fwd

@@ -38,7 +38,7 @@ struct BwdLaunch {
   float* dq_acc;      // workspace: fp32 [B*H, N_q, d]
   float* delta;       // workspace: fp32 [B*H, N_q rounded up to 128], then LSE*log2e, same shape
   unsigned* counters; // workspace: [B*H, N_q / 128 rounded up] dQ contributions applied (deterministic mode)
-  unsigned* ticket;   // workspace: one word, the next CTA ticket (deterministic mode)
+  unsigned* ticket;   // workspace: one word, the next CTA ticket
   int deterministic;
   int BH, N_q, N_kv, d, causal;
   int n_sms;          // multiprocessor count of the device

@@ -17,9 +17,9 @@ namespace {
 
 // Workspace of fa_bwd_noalloc, shared by every call on a device.  Each call
 // clears and rewrites what it uses (the backward's first kernel writes both
-// row vectors and the counters, and the dQ accumulator is cleared before any
-// partial is added to it), so leftover contents from an earlier call do not
-// matter; calls that overlap on the GPU would race on it.
+// row vectors and the counters and clears the dQ accumulator), so leftover
+// contents from an earlier call do not matter; calls that overlap on the GPU
+// would race on it.
 static __device__ __align__(256) unsigned char g_bwd_scratch[FA_BWD_NOALLOC_MAX_WORKSPACE];
 
 // Device address of g_bwd_scratch on the current device.
