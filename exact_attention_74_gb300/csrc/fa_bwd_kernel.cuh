@@ -292,12 +292,20 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       // Fixed order: once a partial has landed, the next key tile may add
       // into that query tile.  The landing wait is taken after this step's
       // loads are issued, so it overlaps them instead of delaying them.
+      // The count only has to order the next key tile's reduce-add after
+      // this one at L2, where both the partials and the count are applied:
+      // the bulk group has completed (L2 has acknowledged this partial)
+      // before the relaxed add on the count is even issued, and the next key
+      // tile issues its partial only after it has read the raised count.
+      // This leans on that completion, not on a release in the PTX memory
+      // model's sense: a GPU-scope release waits behind the loads just
+      // issued and cost the fixed-order mode a tenth of its speed.
       unsigned* release_cnt = nullptr;
       auto release = [&] {
         if (release_cnt == nullptr) return;
         bulk_wait_group0();
         fence_proxy_async_global();
-        red_release_gpu_add(release_cnt, 1u);
+        red_relaxed_gpu_add(release_cnt, 1u);
         release_cnt = nullptr;
       };
       for (int t = 0; t < n_it + 2; ++t) {
