@@ -19,7 +19,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID", "FA_ERR_UNSUPPORTED", "FA_ERR_ALIGN", "FA_ERR_WORKSPACE",
     "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FAError", "library", "library_path",
     "fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "forward_fp8", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_last_device_status",
-    "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE", "fa_bwd_ex",
+    "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE", "fa_bwd_ex", "fa_bwd_pair",
     "fa_set_wait_timeout_ns", "fa_status_string", "fa_test_exp2", "fa_test_mma_tile",
     "fa_test_mma_fp8", "fa_test_wait_timeout", "forward", "backward", "EXPORTED_SYMBOLS",
 ]
@@ -45,6 +45,8 @@ _SIGNATURES = {
                     _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                        _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa_bwd_pair": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                         _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_get_last_device_status": (_i, [_vp]),
@@ -124,6 +126,13 @@ def fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale
               deterministic, workspace, workspace_bytes, stream=0):
     return _call("fa_bwd_ex", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
                  deterministic, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_pair(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
+                workspace, workspace_bytes, stream=0):
+    """fa_bwd at d = 64 on pairs of thread blocks sharing 256-key products."""
+    return _call("fa_bwd_pair", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale,
+                 workspace, workspace_bytes, stream)
 
 
 # Bytes of scratch fa_bwd_noalloc can use (FA_BWD_NOALLOC_MAX_WORKSPACE in fa.h).
@@ -235,8 +244,10 @@ def forward_fp8(q, k, v, causal=False, scale=None, signs=None, out=None, lse=Non
 
 
 def backward(q, k, v, o, do, lse, causal=False, scale=None, stream=None, workspace=None,
-             deterministic=False):
-    """dQ, dK, dV for bf16 tensors [B, H, N, d] and fp32 LSE [B, H, N_q]."""
+             deterministic=False, pair=False):
+    """dQ, dK, dV for bf16 tensors [B, H, N, d] and fp32 LSE [B, H, N_q].
+
+    pair=True runs fa_bwd_pair (d = 64 only; not with deterministic)."""
     import torch
     B, H, N_q, d = q.shape
     N_kv = k.shape[2]
@@ -247,10 +258,15 @@ def backward(q, k, v, o, do, lse, causal=False, scale=None, stream=None, workspa
     need = fa_bwd_workspace_bytes(B, H, N_q, N_kv, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                   B, H, N_q, N_kv, d, int(causal), scale, int(deterministic), workspace.data_ptr(),
-                   workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if pair:
+        if deterministic:
+            raise ValueError("pair=True has no fixed-order mode")
+        st = fa_bwd_pair(*ptrs, B, H, N_q, N_kv, d, int(causal), scale, *ws)
+    else:
+        st = fa_bwd_ex(*ptrs, B, H, N_q, N_kv, d, int(causal), scale, int(deterministic), *ws)
     if st != FA_OK:
-        raise FAError(st, "fa_bwd")
+        raise FAError(st, "fa_bwd_pair" if pair else "fa_bwd")
     return dq, dk, dv

@@ -161,6 +161,22 @@ int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// The same bf16 tensor in boxes of 32 columns (64 bytes) x box_rows x 1 with
+// 64-byte swizzle: one half of a d = 64 row per box.
+int make_map_bf16_sw64(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // 3-D map over a contiguous u8 [BH, rows, inner] tensor (inner a multiple of
 // 128): 128 x 128 x 1 boxes, 128-byte swizzle.
 int make_map_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int BH) {
@@ -324,12 +340,13 @@ namespace fa {
 // checked as one.
 int bwd_entry(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
               void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
-              int deterministic, void* workspace, size_t workspace_bytes, bool internal_workspace,
+              int deterministic, bool pair, void* workspace, size_t workspace_bytes, bool internal_workspace,
               cudaStream_t stream) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID;
   int st = check_sizes(B, H, N_q, N_kv, d, causal, scale);
   if (st != FA_OK) return st;
   if (d == 256) return FA_ERR_UNSUPPORTED;   // the backward kernel covers d = 64 and 128
+  if (pair && d != 64) return FA_ERR_UNSUPPORTED;   // the pair kernel covers d = 64
   if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID;
   if (misaligned(Q, 16) || misaligned(K, 16) || misaligned(V, 16) || misaligned(O, 16) ||
       misaligned(dO, 16) || misaligned(dQ, 16) || misaligned(dK, 16) || misaligned(dV, 16) ||
@@ -349,6 +366,13 @@ int bwd_entry(const void* Q, const void* K, const void* V, const void* O, const 
   if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmdO, dO, d, N_q, BH)) != FA_OK) return st;
   if ((st = make_map_f32(&a.tmDQ, workspace, d, N_q, BH, 32, 32)) != FA_OK) return st;
+  if (pair) {
+    if ((st = make_map_bf16(&a.tmQh, Q, d, N_q, BH, 64)) != FA_OK) return st;
+    if ((st = make_map_bf16(&a.tmdOh, dO, d, N_q, BH, 64)) != FA_OK) return st;
+    if ((st = make_map_bf16_sw64(&a.tmQc, Q, d, N_q, BH, 128)) != FA_OK) return st;
+    if ((st = make_map_bf16_sw64(&a.tmdOc, dO, d, N_q, BH, 128)) != FA_OK) return st;
+    if ((st = make_map_bf16_sw64(&a.tmKc, K, d, N_kv, BH, 128)) != FA_OK) return st;
+  }
   const size_t rows = static_cast<size_t>(BH) * N_q;
   a.o = O;
   a.dO = dO;
@@ -372,7 +396,7 @@ int bwd_entry(const void* Q, const void* K, const void* V, const void* O, const 
   a.causal = causal;
   a.scale = scale;
   a.stream = stream;
-  const cudaError_t e = launch_bwd(a);
+  const cudaError_t e = pair ? launch_bwd_pair(a) : launch_bwd(a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
@@ -387,7 +411,14 @@ extern "C" {
 int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
               void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
               int deterministic, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  return bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, deterministic, workspace,
+  return bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, deterministic, false,
+                   workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_pair(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+                void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, 0, true, workspace,
                    workspace_bytes, false, static_cast<cudaStream_t>(stream));
 }
 

@@ -29,6 +29,9 @@ cudaError_t launch_fwd_d256(const FwdLaunch& a);   // 64-row K/V boxes
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO;   // same map shape as the forward's
   CUtensorMap tmDQ;                  // fp32 dQ accumulator (d, N_q, B*H), 32 x 32 x 1 boxes
+  // pair kernel only (d = 64): Q and dO in 64-row boxes (128-byte swizzle),
+  // Q, dO and K in 32-column boxes of 128 rows (64-byte swizzle)
+  CUtensorMap tmQh, tmdOh, tmQc, tmdOc, tmKc;
   const void* o;
   const void* dO;
   const float* lse;
@@ -48,6 +51,8 @@ struct BwdLaunch {
 };
 
 cudaError_t launch_bwd(const BwdLaunch& a);
+// The backward at d = 64 on pairs of CTAs sharing 256-key products.
+cudaError_t launch_bwd_pair(const BwdLaunch& a);
 
 // The 8-bit forward (d = 128): quantisation into the workspace, then the
 // attention kernel on the e4m3 copies.
@@ -76,13 +81,16 @@ cudaError_t launch_fwd_fp8(const Fp8Launch& a);
 
 // Defined in fa_api.cu.
 int device_ctl(DevCtl* ctl, int* n_sms = nullptr);
-// The backward entry point's checks and launches; internal_workspace = the
-// library's own scratch array (not checked as a caller allocation).
+// The backward entry point's checks and launches; pair = the kernel on pairs
+// of CTAs (d = 64 only); internal_workspace = the library's own scratch array
+// (not checked as a caller allocation).
 int bwd_entry(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
               void* dQ, void* dK, void* dV, int B, int H, int N_q, int N_kv, int d, int causal, float scale,
-              int deterministic, void* workspace, size_t workspace_bytes, bool internal_workspace,
+              int deterministic, bool pair, void* workspace, size_t workspace_bytes, bool internal_workspace,
               cudaStream_t stream);
 int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows = 128);
+// Same tensor, 32-column x box_rows boxes with 64-byte swizzle.
+int make_map_bf16_sw64(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_rows);
 int make_map_f32(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_cols, int box_rows);
 // 3-D map over a contiguous u8 [BH, rows, inner] tensor, 128 x 128 x 1 boxes, 128-byte swizzle.
 int make_map_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int BH);

@@ -42,7 +42,7 @@ extern "C" int fa_bwd_noalloc(const void* Q, const void* K, const void* V, const
   // Argument checks: the backward with no workspace checks every other argument
   // first and returns FA_ERR_WORKSPACE only when they are all valid; it
   // launches nothing and makes no CUDA call on that path.
-  const int st = fa::bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, 0, nullptr, 0,
+  const int st = fa::bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, 0, false, nullptr, 0,
                                false, static_cast<cudaStream_t>(stream));
   if (st != FA_ERR_WORKSPACE) return st;
   const size_t need = fa_bwd_workspace_bytes(B, H, N_q, N_kv, d);
@@ -50,6 +50,6 @@ extern "C" int fa_bwd_noalloc(const void* Q, const void* K, const void* V, const
   void* ws = nullptr;
   const int sa = fa::scratch_address(&ws);
   if (sa != FA_OK) return sa;
-  return fa::bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, 0, ws,
+  return fa::bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N_q, N_kv, d, causal, scale, 0, false, ws,
                        FA_BWD_NOALLOC_MAX_WORKSPACE, true, static_cast<cudaStream_t>(stream));
 }

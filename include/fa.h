@@ -181,6 +181,24 @@ int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O,
               fa_stream_t stream);
 
 /*
+ * fa_bwd_pair -- fa_bwd at head dimension 64 on pairs of thread blocks that
+ * share their tensor-core products ("論文解説: FlashAttention-4 ...",
+ * Backwardパスの最適化, item 2: 2-CTA MMA mode, 256-row tiles across two
+ * CTAs).  Each pair of blocks (a cluster of two) owns 256 keys; every product
+ * is one instruction for both blocks, and each 128-row query tile receives
+ * one fp32 dQ partial per 256 keys instead of one per 128, so the dQ
+ * reduce-adds into the workspace halve.  The result is the same gradient as
+ * fa_bwd's up to the order of fp32 additions; the dQ reduction order is not
+ * fixed (as fa_bwd, not fa_bwd_ex's fixed order).
+ * Arguments, workspace (fa_bwd_workspace_bytes) and errors are those of
+ * fa_bwd; d other than 64 returns FA_ERR_UNSUPPORTED.
+ */
+int fa_bwd_pair(const void* Q, const void* K, const void* V, const void* O,
+                const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                int B, int H, int N_q, int N_kv, int d, int causal, float scale,
+                void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
  *
  * (The pages describe no such call; it is an interface convenience.)  Some

@@ -189,6 +189,23 @@ def test_bwd_ex_deterministic_flag(lib):
         == fa.FA_ERR_WORKSPACE
 
 
+def test_bwd_pair_argument_errors(lib):
+    need = fa.fa_bwd_workspace_bytes(1, 2, 100, 90, 64)
+
+    def call(d=64, ws=P, nbytes=need, dQ=P, causal=1, K=P):
+        return fa.fa_bwd_pair(P, K, P, P, P, P, dQ, P, P, 1, 2, 100, 90, d, causal, 0.125, ws, nbytes, 0)
+
+    # the pair kernel covers d = 64 only; the other argument errors are fa_bwd's
+    assert call(d=128, nbytes=fa.fa_bwd_workspace_bytes(1, 2, 100, 90, 128)) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=256, nbytes=1 << 20) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(dQ=None) == fa.FA_ERR_INVALID
+    assert call(causal=2) == fa.FA_ERR_INVALID
+    assert call(K=P + 8) == fa.FA_ERR_ALIGN
+    assert call(ws=None) == fa.FA_ERR_WORKSPACE
+    assert call(nbytes=need - 1) == fa.FA_ERR_WORKSPACE
+
+
 def test_fp8_workspace_bytes(lib):
     # Q, K and V codes (rows padded to 128), the Q and K multipliers, the
     # block and head maxima of |V|, each rounded up to 256 bytes
