@@ -15,7 +15,8 @@ end-to-end figure through the Python API with pinned host buffers, SM clocks
 sampled during the timed region, every stated workload timed on its own
 ("configs": the tiny case, B4 H16 N4096 in both masks and both passes, the
 16k-token sequence sweep, the rescaling stress case, the causal N8192
-backward in both reduction orders) with the forward gate at N >= 8k, and the
+backward in both reduction orders, the d = 64 backward on single CTAs and on
+CTA pairs) with the forward gate at N >= 8k, and the
 fp64 CPU oracle timed on a bounded sample (cpu_baseline).
 
 ``--impl reference`` times the oracle instead (host cores, bounded sample per
@@ -614,14 +615,14 @@ def fp8_fwd_tflops(torch, fa, w, q, k, v, stream, reps=20):
 def _config_workloads():
     """(label, workload, passes) for every stated workload, then the extra
     head dimensions.  Passes: "fwd", "bwd" (unordered dQ), "bwd_det" (fixed
-    order)."""
+    order), "bwd_pair" (fa_bwd_pair: pairs of CTAs sharing products, d = 64)."""
     W = fa_inputs.WORKLOADS
     out = [("1 tiny", W["tiny"], ("fwd",)), ("1 tiny", W["tiny_causal"], ("fwd",)),
            ("2", W["fwd_4k"], ("fwd", "bwd", "bwd_det")), ("2", W["fwd_4k_causal"], ("fwd", "bwd"))]
     out += [("3 sweep", x, ("fwd",)) for x in fa_inputs.sweep_workloads(False) + fa_inputs.sweep_workloads(True)]
     out += [("4 stress", W["stress_8k"], ("fwd",)), ("5 backward", W["bwd_8k"], ("fwd", "bwd", "bwd_det"))]
-    out += [("extra d=64", W["hdim64_8k"], ("fwd", "bwd")),
-            ("extra d=64", W["hdim64_8k"].with_(name="hdim64_8k_causal", causal=True), ("fwd", "bwd")),
+    out += [("extra d=64", W["hdim64_8k"], ("fwd", "bwd", "bwd_pair")),
+            ("extra d=64", W["hdim64_8k"].with_(name="hdim64_8k_causal", causal=True), ("fwd", "bwd", "bwd_pair")),
             ("extra d=256", W["hdim256_8k"], ("fwd",)), ("extra d=256", W["hdim256_8k_causal"], ("fwd",))]
     return out
 
@@ -664,18 +665,22 @@ def time_configs(torch, fa, dev, stream, peak, reps=10):
             ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
             for p in bwd_passes:
                 det = 1 if p == "bwd_det" else 0
+                args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N_q, w.N_kv, w.d, int(w.causal),
+                        w.scale)
 
                 def bwd():
-                    st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H,
-                                      w.N_q, w.N_kv, w.d, int(w.causal), w.scale, det, ws.data_ptr(), wsb, sh)
+                    if p == "bwd_pair":
+                        st = fa.fa_bwd_pair(*args, ws.data_ptr(), wsb, sh)
+                    else:
+                        st = fa.fa_bwd_ex(*args, det, ws.data_ptr(), wsb, sh)
                     if st != fa.FA_OK:
-                        raise fa.FAError(st, f"fa_bwd_ex {w.name}")
+                        raise fa.FAError(st, f"{p} {w.name}")
 
                 ms = statistics.median(event_times(torch, stream, bwd, reps))
                 tf = w.bwd_flops() / (ms * 1e-3) / 1e12
-                out.append({**rec, "pass": "bwd fixed order" if det else "bwd", "ms": ms, "tflops": tf,
-                            "frac": tf / peak})
+                name = {"bwd": "bwd", "bwd_det": "bwd fixed order", "bwd_pair": "bwd cta pair"}[p]
+                out.append({**rec, "pass": name, "ms": ms, "tflops": tf, "frac": tf / peak})
             del do, dq, dk, dv, ws
         del o, lse
     torch.cuda.synchronize(dev)
@@ -753,7 +758,7 @@ def run_profile_case(args):
                             emu_per_32=None if args.emu is None else args.emu)
         if not args.fwd_only:
             fa.backward(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, workspace=ws,
-                        deterministic=args.deterministic)
+                        deterministic=args.deterministic, pair=args.pair)
     e1.record()
     torch.cuda.synchronize()
     st = fa.fa_get_last_device_status(torch.cuda.current_stream().cuda_stream)
@@ -779,6 +784,7 @@ def main():
     ap.add_argument("--fwd-only", action="store_true", help="with --profile: forward only")
     ap.add_argument("--fp8", action="store_true", help="with --profile: the 8-bit forward only")
     ap.add_argument("--deterministic", action="store_true", help="with --profile: the fixed-order backward")
+    ap.add_argument("--pair", action="store_true", help="with --profile: the backward on CTA pairs (d = 64)")
     ap.add_argument("--emu", type=int, choices=(0, 8, 16), default=None,
                     help="with --profile: exponentials per 32 on the FMA-pipe emulation (default: the library's)")
     args = ap.parse_args()

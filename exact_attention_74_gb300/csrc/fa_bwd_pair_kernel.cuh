@@ -315,8 +315,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUt
     // One arrival into the leader: each thread of the leader (its products
     // read only its own tensor and shared memory for these signals, so a
     // CTA-scope release is enough, or none for completed tensor-memory
-    // reads), each warp of CTA 1 once.  CTA 1's arrivals carry a cluster-scope
-    // release only where its warps' own shared-memory writes must be seen.
+    // reads), each warp of CTA 1 once, after every lane's tensor-memory
+    // stores (tcgen05 fence) or shared-memory writes (async-proxy fence) and
+    // the warp barrier.  CTA 1's arrival releases at cluster scope only
+    // where its warps' own shared-memory writes are read next (a release at
+    // that scope costs about half a microsecond per arrival).
     auto signal_leader = [&](int b, bool smem_writes) {
       if (leader) {
         if (b == bDQFree || b == bDQFree + 1) mbar_arrive_relaxed(bar(b));
@@ -421,7 +424,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUt
         tmem_st_x16(tmem + lane_addr + kColS + 16 * 3, pk_keep[1]);
       }
       tc_fence_before();
-      signal_leader(bP, false);               // dV may use P now
+      signal_leader(bP, false);        // dV may use P now
       // ---- dS = P o (dP - D), once dP is ready
       if (ok) ok = wait(bDP, it);
       ok = __all_sync(0xffffffffu, ok);
@@ -452,7 +455,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUt
       tmem_st_x16(tmem + lane_addr + kColDS + 32 * half, dsk[0]);
       tmem_st_x16(tmem + lane_addr + kColDS + 32 * half + 16, dsk[1]);
       tc_fence_before();
-      signal_leader(bDST, false);             // dK may read dS^T now
+      signal_leader(bDST, false);      // dK may read dS^T now
       // The same values as rows of dS^T (key 128 rank + r, this warp's 64
       // queries, 4 KB per warp) into the dQ operand of the CTA owning query
       // tile i (CTA it & 1).  The owner writes them in place; CTA 1 (even

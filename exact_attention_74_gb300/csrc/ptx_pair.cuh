@@ -39,22 +39,16 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
                :: "r"(dst), "r"(src), "r"(bytes), "r"(cbar) : "memory");
 }
 
-// Arrive on a barrier of this CTA, releasing at cluster scope (the waiter may
-// go on to read the other CTA's memory through a pair product).
-__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
-}
-
 // Arrive on a barrier in another CTA of the cluster (address from map_shared),
 // releasing this thread's prior shared-memory writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cbar) : "memory");
 }
 
-// The same without release semantics: for hand-offs of tensor memory (which
-// the tcgen05 fences around the arrival order) and of data that has already
-// landed where the waiter's products read it.  A release at cluster scope
-// costs about half a microsecond per arrival on this path.
+// The same without release semantics, for hand-offs of tensor memory
+// (ordered by the tcgen05 fences around the arrival) and of data that has
+// already landed where the waiter's products read it.  A release at cluster
+// scope costs about half a microsecond per arrival.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cbar) : "memory");
 }
