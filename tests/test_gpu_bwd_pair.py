@@ -122,6 +122,46 @@ def test_agrees_with_single_block_backward(torch, causal):
         e = gu.rel_rms(x, y)
         print(f"{w.name}: {name} pair vs single-block rel-RMS {e:.2e}")
         assert e <= 2e-3, f"{name}: {e:.3e}"
+    # dK and dV are the same products over the same query tiles in the same
+    # order (the pair only splits B's columns between the blocks): identical
+    for name, x, y in zip(("dK", "dV"), a[1:], b[1:]):
+        assert np.array_equal(x, y), f"{name}: pair and single-block results differ"
+
+
+def test_two_streams_at_once(torch):
+    """Two pair calls on different streams (own workspaces, inputs and
+    outputs) overlapping on the device: both equal to the same call made
+    alone, dK and dV bit for bit (their order is fixed), dQ within the
+    reordering of its fp32 additions."""
+    ws_ = [_wl(1, 8, 2048, 2048, False, seed=71), _wl(1, 8, 2048, 2048, True, seed=72)]
+    runs = []
+    for w in ws_:
+        qb, kb, vb = fa_inputs.make_qkv(w)
+        t = _forward(torch, w, qb, kb, vb)
+        do = gu.dev_bf16(fa_inputs.make_dout(w))
+        runs.append((w, t, do, _backward(torch, w, t, do)))
+    streams = [torch.cuda.Stream() for _ in runs]
+    outs = []
+    torch.cuda.synchronize()
+    for (w, t, do, _), st in zip(runs, streams):
+        q, k, v, o, lse = t
+        B, H, N, d = q.shape
+        dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+        need = fa.fa_bwd_workspace_bytes(B, H, N, N, d)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        with torch.cuda.stream(st):
+            ws.fill_(0xFF)
+            r = fa.fa_bwd_pair(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, N, d,
+                               int(w.causal), w.scale, ws.data_ptr(), need, st.cuda_stream)
+        assert r == fa.FA_OK
+        outs.append((dq, dk, dv, ws))
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    for (w, _, _, alone), (dq, dk, dv, _) in zip(runs, outs):
+        got = [gu.to_f64(x) for x in (dq, dk, dv)]
+        assert np.array_equal(got[1], alone[1]) and np.array_equal(got[2], alone[2]), w.name
+        assert gu.rel_rms(got[0], alone[0]) <= 1e-4, w.name
 
 
 @pytest.mark.parametrize("causal", [False, True])
