@@ -128,6 +128,32 @@ def test_agrees_with_single_block_backward(torch, causal):
         assert np.array_equal(x, y), f"{name}: pair and single-block results differ"
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_against_single_block(torch, seed):
+    """Seeded random shapes (batch, heads, query and key lengths, mask): the
+    pair backward against the single-block one on the same inputs, dK and dV
+    bit for bit, dQ within the reordering of its fp32 additions; and every
+    gradient against the oracle on one head."""
+    rng = np.random.default_rng(1000 + seed)
+    B, H = int(rng.integers(1, 3)), int(rng.integers(1, 5))
+    causal = bool(rng.integers(0, 2))
+    N_q = int(rng.integers(1, 1300))
+    N_kv = N_q if rng.integers(0, 2) else int(rng.integers(1, 1300))
+    w = _wl(B, H, N_q, N_kv, causal, seed=2000 + seed)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    t = _forward(torch, w, qb, kb, vb)
+    do = gu.dev_bf16(dob)
+    a = _backward(torch, w, t, do, pair=True)
+    b = _backward(torch, w, t, do, pair=False)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2]), w.name
+    assert gu.rel_rms(a[0], b[0]) <= 1e-4, w.name
+    bi, hi = B - 1, H - 1
+    q, k, v, dO = (fa_inputs.bf16_bits_to_f64(x[bi, hi]) for x in (qb, kb, vb, dob))
+    ref = oracle.head_backward(q, k, v, dO, causal=causal, scale=w.scale)
+    _check((a[0][bi, hi], a[1][bi, hi], a[2][bi, hi]), ref, f"{w.name} b{bi} h{hi}")
+
+
 def test_two_streams_at_once(torch):
     """Two pair calls on different streams (own workspaces, inputs and
     outputs) overlapping on the device: both equal to the same call made
