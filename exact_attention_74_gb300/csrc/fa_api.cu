@@ -239,6 +239,7 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH, kv_rows)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH, kv_rows)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmO, O, d, N_q, BH, 32)) != FA_OK) return st;
   a.o = O;
   a.lse = LSE;
   a.BH = BH;

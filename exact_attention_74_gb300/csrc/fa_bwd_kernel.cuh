@@ -267,6 +267,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     *logical_slot = b;
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -682,6 +683,7 @@ main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
   }
 
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

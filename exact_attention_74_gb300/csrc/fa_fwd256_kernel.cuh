@@ -129,6 +129,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init_fence();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -346,6 +347,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
   }
 
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -63,7 +63,7 @@ __device__ constexpr uint32_t col_O(int t) { return 256u * t + 192u; }
 template <int EMU, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-             const __grid_constant__ CUtensorMap tmV, const Params p) {
+             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -106,6 +106,7 @@ fwd64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     mbar_init_fence();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -354,7 +355,10 @@ fwd64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       hand_back(2 * nt - 1);                  // V of the last step
       tc_fence_after();
       const float inv_l = 1.f / (l + lr);
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
+      // O (bf16) of this warp's 32 rows into the tile's Q buffer, dead since
+      // the tile's last S, as a 128-byte-swizzled TMA box (64 columns x 32
+      // rows); lane 0 stores it (rows past N_q are clipped by the tensor map)
+      uint8_t* rowp = smem + kQOff + t * kTileBytes + r_in_tile * 128;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
@@ -363,17 +367,24 @@ fwd64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (row < p.N_q) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(rowp + (((4 * ch + i) ^ (r_in_tile & 7)) * 16)) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tmO, sb + kQOff + t * kTileBytes + rank * 32 * 128, 0, qbase0 + t * kBM + rank * 32, bh);
+        bulk_commit_group();
       }
       if (row < p.N_q)
         p.lse[static_cast<size_t>(bh) * p.N_q + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
     }
   }
 
+  if (warp >= 2 && warp <= 9 && lane == 0) bulk_wait_group_read<0>();   // O's box has been read
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -401,7 +412,7 @@ cudaError_t launch(const FwdLaunch& a) {
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_qpairs) * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmO, p);
   return cudaGetLastError();
 }
 

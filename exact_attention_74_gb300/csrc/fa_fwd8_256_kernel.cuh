@@ -118,6 +118,7 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init_fence();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -317,6 +318,7 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
   }
 
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -117,7 +117,7 @@ __device__ __forceinline__ float ex2_mix(float x, int col) {
 template <int D, int EMU, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-           const __grid_constant__ CUtensorMap tmV, const Params p) {
+           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -160,6 +160,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     mbar_init_fence();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -449,7 +450,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (__all_sync(0xffffffffu, ready)) {
       tc_fence_after();
       const float inv_l = 1.f / (l + lr);
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N_q + row) * D;
+      // O (bf16) of this warp's 32 rows into the tile's Q buffer, dead since
+      // the tile's last S, in the 128-byte-swizzled layout of a TMA box
+      // (64 columns x 32 rows per panel); lane 0 stores the boxes (rows
+      // past N_q are clipped by the tensor map).  The buffer and row in the
+      // tile come from a fresh read of the thread index: values that live
+      // through the key loop only for this would take registers there.
+      const uint32_t tid = tid_x_fresh();
+      const uint32_t r_tile = tid & 127;                   // row in the query tile
+      const uint32_t buf = C::kQOff + ((tid - 64) >> 7) * C::kTileBytes;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
@@ -458,17 +467,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (row < p.N_q) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * ch);
+        // columns 32 ch .. 32 ch + 31: panel ch / 2, 16-byte chunks 4 (ch & 1) .. + 3
+        uint8_t* rowp = smem + buf + (ch >> 1) * kPanelBytes + r_tile * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(rowp + (((4 * (ch & 1) + i) ^ (r_tile & 7)) * 16)) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_store_3d(&tmO, sb + buf + pn * kPanelBytes + (r_tile & ~31u) * 128, 64 * pn, row - lane, bh);
+        bulk_commit_group();
       }
       if (row < p.N_q)
         p.lse[static_cast<size_t>(bh) * p.N_q + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
     }
   }
 
+  if (warp >= 2 && lane == 0) bulk_wait_group_read<0>();   // O's boxes have been read
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -497,7 +516,7 @@ cudaError_t launch(const FwdLaunch& a) {
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_qpairs) * p.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmO, p);
   return cudaGetLastError();
 }
 

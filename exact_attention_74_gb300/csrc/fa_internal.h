@@ -12,6 +12,7 @@ namespace fa {
 struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV;   // 3-D maps (d, N, B*H), 64 x 128 x 1 boxes (K, V: 64 x 64 at d = 256),
                                // 128 B swizzle
+  CUtensorMap tmO;             // O (d, N_q, B*H), 64 x 32 x 1 boxes, 128 B swizzle (d = 64, 128 stores)
   void* o;
   float* lse;
   int BH, N_q, N_kv, d, causal;

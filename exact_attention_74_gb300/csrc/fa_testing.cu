@@ -43,6 +43,7 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 256);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -76,6 +77,7 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     tc_fence_before();
   }
+  __syncwarp();
   __syncthreads();
   if (threadIdx.x == 0) {
     tc_fence_after();
@@ -107,6 +109,7 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
   }
   (void)lane;
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -123,6 +126,7 @@ __global__ void wait_timeout_kernel(DevCtl ctl) {
     abort_flag = 0;
     mbar_init_fence();
   }
+  __syncwarp();
   __syncthreads();
   // Nothing ever arrives on `bar`: the bounded wait runs out and flags it.
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, ctl, &abort_flag);
@@ -148,6 +152,7 @@ mma_fp8_kernel(const float* A, const float* B, float* Cout, uint8_t* a_codes, in
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 256);
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -167,6 +172,7 @@ mma_fp8_kernel(const float* A, const float* B, float* Cout, uint8_t* a_codes, in
   }
   if (mode == 1) tmem_st_x32(tmem + lane_addr + 128, wa);
   fence_async_smem();
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (r == 0) {
@@ -191,6 +197,7 @@ mma_fp8_kernel(const float* A, const float* B, float* Cout, uint8_t* a_codes, in
       for (int i = 0; i < 32; ++i) Cout[r * 128 + 32 * ch + i] = __uint_as_float(v[i]);
     }
   }
+  __syncwarp();   // warps whose lane 0 ran a role alone arrive whole
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
