@@ -9,11 +9,17 @@
 //                   Q as bf16 pairs [128,256) (copied in once), O [256,512)
 //   warp 0          TMA producer: Q once (64 KB), then K_j, V_j (32 KB each)
 //                   into a ring of five shared-memory slots
-//   warp 1          MMA issuer (one thread): S_{j+1} = Q K_{j+1}^T (A from
-//                   tensor memory, so only K is read from shared memory) is
-//                   queued before O += P_j V_j, so the tensor core computes
+//   warp 1          issues S_{j+1} = Q K_{j+1}^T (A from tensor memory, so only
+//                   K is read from shared memory) as soon as K_{j+1} is in and
+//                   P V_{j-1} has read its buffer, so the tensor core computes
 //                   the next scores while the softmax of the current ones runs
+//   warp 6          issues O += P_j V_j once P_j is written
 //   warps 2-5       softmax, one thread per query row (one tensor-memory lane)
+//
+// One thread sends the tensor core a product only every ~100 cycles, about
+// what an N = 64 product takes whatever its shape, and a step's sixteen
+// S products (K = 256) alone fill that; with the P V products on a thread of
+// their own the two streams run side by side.
 //
 // The per-row recurrence is the same online softmax in base 2 with the
 // conditional rescaling of "論文解説: FlashAttention-4 — Algorithm and Kernel
@@ -37,7 +43,7 @@ namespace fwd256 {
 constexpr int D = 256;
 constexpr int kBM = 128;                  // query rows per CTA
 constexpr int kBN = 64;                   // keys per step
-constexpr int kThreads = 192;             // 6 warps
+constexpr int kThreads = 224;             // 7 warps
 constexpr int kSlots = 5;                 // K/V ring
 constexpr int kQPanel = 128 * 128;        // 128 rows x 128 B (64 bf16) swizzle panel
 constexpr int kKPanel = 64 * 128;         // 64 rows x 128 B
@@ -54,7 +60,8 @@ constexpr int kKVEmpty = 2 + kSlots;      // kSlots
 constexpr int kSFull = 2 + 2 * kSlots;    // 2 (per S buffer)
 constexpr int kPFull = 4 + 2 * kSlots;    // 2 (per S buffer)
 constexpr int kOFull = 6 + 2 * kSlots;
-constexpr int kNumBars = 7 + 2 * kSlots;
+constexpr int kPVDone = 7 + 2 * kSlots;   // 2 (per S buffer): P V has read the buffer's P
+constexpr int kNumBars = 9 + 2 * kSlots;
 constexpr int kMiscOff = kBarOff + 8 * kNumBars;   // tmem base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + base alignment slack
 // tensor-memory columns
@@ -125,6 +132,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(bar(kPFull + b), 4);        // one arrive per softmax warp
     }
     mbar_init(bar(kOFull), 1);
+    mbar_init(bar(kPVDone + 0), 1);
+    mbar_init(bar(kPVDone + 1), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -155,54 +164,47 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                            (i >> 1) * kBN, bh, keep);
       }
     }
-  } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    // ---------------------------------------------- MMA issuers (S; P V)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       auto slot_addr = [&](int i) { return sb + kKVOff + ring_slot(i) * kSlotBytes; };
       auto kv_wait = [&](int i) { return mbar_wait(bar(kKVFull + ring_slot(i)), ring_phase(i), p.ctl, abort_flag); };
-      auto issue_S = [&](int j) {          // S_j = Q K_j^T into S buffer j & 1
-        const uint32_t ka = slot_addr(2 * j);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ts(tmem + kColS + 64 * (j & 1), tmem + kColQ + 8 * k,
-                 sdesc_sw128(ka + (k >> 2) * kKPanel + (k & 3) * 32, 0, 1024), idS, k > 0 ? 1u : 0u);
-      };
-      auto issue_PV = [&](int j) {         // O += P_j V_j, P_j over S buffer j & 1
-        const uint32_t va = slot_addr(2 * j + 1);
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          mma_ts(tmem + kColO, tmem + kColS + 64 * (j & 1) + 8 * k, sdesc_sw128(va + k * 2048, kKPanel, 1024),
-                 idO, (j > 0 || k > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar(kQReady), 0, p.ctl, abort_flag);
-      if (ok) ok = kv_wait(0);
-      if (ok) {
-        tc_fence_after();
-        issue_S(0);
-        tc_commit(bar(kSFull + 0));
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        if (j + 1 < n) {
-          // the next scores first; their buffer held P_{j-1}, which the P V
-          // queued in the previous step has read
-          if (!(ok = kv_wait(2 * j + 2))) break;
+      bool ok = true;
+      if (warp == 1) {
+        ok = mbar_wait(bar(kQReady), 0, p.ctl, abort_flag);
+        for (int j = 0; j < n && ok; ++j) {   // S_j = Q K_j^T into S buffer j & 1
+          if (!(ok = kv_wait(2 * j))) break;
+          // the buffer held P_{j-2}: P V_{j-2} must have read it
+          if (j >= 2 && !(ok = mbar_wait(bar(kPVDone + (j & 1)), ((j - 2) >> 1) & 1, p.ctl, abort_flag))) break;
           tc_fence_after();
-          issue_S(j + 1);
-          tc_commit(bar(kSFull + ((j + 1) & 1)));
+          const uint32_t ka = slot_addr(2 * j);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ts(tmem + kColS + 64 * (j & 1), tmem + kColQ + 8 * k,
+                   sdesc_sw128(ka + (k >> 2) * kKPanel + (k & 3) * 32, 0, 1024), idS, k > 0 ? 1u : 0u);
+          tc_commit(bar(kSFull + (j & 1)));
+          tc_commit(bar(kKVEmpty + ring_slot(2 * j)));        // K_j read
         }
-        tc_commit(bar(kKVEmpty + ring_slot(2 * j)));          // K_j: read by S_j, queued before
-        if (!(ok = kv_wait(2 * j + 1))) break;
-        if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
-        tc_fence_after();
-        issue_PV(j);
-        tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));      // V_j (and: P V_j is complete)
+      } else {
+        for (int j = 0; j < n && ok; ++j) {   // O += P_j V_j, P_j over S buffer j & 1
+          if (!(ok = kv_wait(2 * j + 1))) break;
+          if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t va = slot_addr(2 * j + 1);
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            mma_ts(tmem + kColO, tmem + kColS + 64 * (j & 1) + 8 * k, sdesc_sw128(va + k * 2048, kKPanel, 1024),
+                   idO, (j > 0 || k > 0) ? 1u : 0u);
+          tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));    // V_j (and: P V_j is complete)
+          tc_commit(bar(kPVDone + (j & 1)));
+        }
+        if (ok) tc_commit(bar(kOFull));
       }
-      if (ok) tc_commit(bar(kOFull));
     }
   } else {
-    // -------------------------------------------------------------- softmax
+    // ------------------------------------------------------- softmax (2-5)
     const int rank = warp & 3;              // tensor-memory lane quarter
     const int r_in_tile = rank * 32 + lane;
     const int row = qbase + r_in_tile;
