@@ -190,6 +190,30 @@ def test_full_size_backward(torch):
         check_grads((dq[b, h], dk[b, h], dv[b, h]), ref, f"{w.name} b{b} h{h}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_heads_d64(torch, causal):
+    """d = 64 on B*H = 600 heads of 200 rows: many CTAs of the unordered d = 64
+    kernel in flight, heads interleaved in a wave, a ragged last tile."""
+    full_compare(torch, _wl(2, 300, 200, 200, 64, causal, seed=31))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_size_d64(torch, causal):
+    """The d = 64 workload B2 H16 N8192 at full size through fa_bwd (the
+    unordered d = 64 kernel: every intermediate in its own tensor-memory
+    columns, products on two issuing threads): dQ, dK, dV of four whole heads
+    (both batches, first and last heads among them) against the oracle's exact
+    gradients."""
+    w = fa_inputs.WORKLOADS["hdim64_8k"].with_(causal=causal)
+    qb, kb, vb = fa_inputs.make_qkv(w)
+    dob = fa_inputs.make_dout(w)
+    dq, dk, dv = run_fwd_bwd(torch, w, qb, kb, vb, dob)
+    for b, h in ((0, 0), (0, 9), (1, 4), (1, 15)):
+        q, k, v, do = (fa_inputs.bf16_bits_to_f64(x[b, h]) for x in (qb, kb, vb, dob))
+        ref = oracle.head_backward(q, k, v, do, causal=w.causal, scale=w.scale)
+        check_grads((dq[b, h], dk[b, h], dv[b, h]), ref, f"{w.name} c{int(causal)} b{b} h{h}")
+
+
 # ----------------------------------------------------------- deterministic mode
 
 def _bwd_ex(torch, w, t, deterministic):
