@@ -14,8 +14,8 @@
 //   dQ [320, 384), dV [384, 448), dK [448, 512)
 // with dK taking dS^T from shared memory (the buffer dQ reads, as a K-major
 // operand) rather than from tensor memory.  Two threads issue the products
-// (one thread sends the tensor core a product only every ~100 cycles, and
-// a step has 32 of them):
+// (on one, the waits for P, dS and the drained dQ would hold back products
+// whose own inputs are ready):
 //   warp 1   S_{i+1}  as soon as the compute warps have read S_i,
 //            dV_i     once P_i is written (and dO_i has landed),
 //            dK_i     once dS_i is in shared memory;

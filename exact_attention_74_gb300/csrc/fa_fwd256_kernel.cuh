@@ -16,10 +16,9 @@
 //   warp 6          issues O += P_j V_j once P_j is written
 //   warps 2-5       softmax, one thread per query row (one tensor-memory lane)
 //
-// One thread sends the tensor core a product only every ~100 cycles, about
-// what an N = 64 product takes whatever its shape, and a step's sixteen
-// S products (K = 256) alone fill that; with the P V products on a thread of
-// their own the two streams run side by side.
+// With one thread issuing both, the next S waited behind that thread's wait
+// for P and its P V products; on threads of their own, each stream goes out
+// as soon as its own inputs are ready.
 //
 // The per-row recurrence is the same online softmax in base 2 with the
 // conditional rescaling of "論文解説: FlashAttention-4 — Algorithm and Kernel
