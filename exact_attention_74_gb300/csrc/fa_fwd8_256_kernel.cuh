@@ -12,11 +12,14 @@
 //                   O [256,512)
 //   warp 0          TMA producer: the Q codes once (32 KB), then K_j, V_j
 //                   (32 KB each: two 128-byte panels) into a five-slot ring
-//   warp 1          MMA issuer: S_{j+1} = Q K_{j+1}^T (both operands in
-//                   shared memory, eight kind::f8f6f4 products of K = 32) is
-//                   queued before O += P_j V_j (four products of N = 256, V
-//                   as the MN-major operand), so the tensor core computes the
-//                   next scores while the softmax of the current ones runs
+//   warp 1          issues S_{j+1} = Q K_{j+1}^T (both operands in shared
+//                   memory, eight kind::f8f6f4 products of K = 32) as soon as
+//                   K_{j+1} is in and P V_{j-1} has read its buffer, so the
+//                   tensor core computes the next scores while the softmax of
+//                   the current ones runs
+//   warp 6          issues O += P_j V_j (four products of N = 256, V as the
+//                   MN-major operand) once P_j is written; on one thread the
+//                   next S would wait behind the wait for P_j
 //   warps 2-5       softmax, one thread per query row: S_j scaled by
 //                   c = scale log2(e) / (inv_q inv_k_j), the online softmax
 //                   with conditional rescaling, P rounded to e4m3
@@ -35,7 +38,7 @@ namespace fwd8_256 {
 constexpr int D = 256;
 constexpr int kBM = 128;                  // query rows per CTA
 constexpr int kBN = 128;                  // keys per step: one quantisation block
-constexpr int kThreads = 192;             // 6 warps
+constexpr int kThreads = 224;             // 7 warps
 constexpr int kSlots = 5;                 // K/V ring
 constexpr int kPanel = 128 * 128;         // 128 rows x 128 B swizzle panel
 constexpr int kTileBytes = 2 * kPanel;    // 128 rows x 256 B
@@ -49,7 +52,8 @@ constexpr int kKVEmpty = 1 + kSlots;      // kSlots
 constexpr int kSFull = 1 + 2 * kSlots;    // 2 (per S buffer)
 constexpr int kPFull = 3 + 2 * kSlots;    // 2 (per S buffer)
 constexpr int kOFull = 5 + 2 * kSlots;
-constexpr int kNumBars = 6 + 2 * kSlots;
+constexpr int kPVDone = 6 + 2 * kSlots;   // 2 (per S buffer): P V has read the buffer's P
+constexpr int kNumBars = 8 + 2 * kSlots;
 constexpr int kMiscOff = kBarOff + 8 * kNumBars;   // tmem base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + base alignment slack
 // tensor-memory columns
@@ -114,6 +118,8 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar(kPFull + b), 4);        // one arrive per softmax warp
     }
     mbar_init(bar(kOFull), 1);
+    mbar_init(bar(kPVDone + 0), 1);
+    mbar_init(bar(kPVDone + 1), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -144,59 +150,52 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                            (i >> 1) * kBN, bh, keep);
       }
     }
-  } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    // ---------------------------------------------- MMA issuers (S; P V)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_e4m3(kBM, kBN);            // S = Q K^T, both K-major
       constexpr uint32_t idO = idesc_e4m3(kBM, D, true);        // O += P V, V MN-major
       auto slot_addr = [&](int i) { return sb + kKVOff + ring_slot(i) * kTileBytes; };
       auto kv_wait = [&](int i) { return mbar_wait(bar(kKVFull + ring_slot(i)), ring_phase(i), p.ctl, abort_flag); };
-      auto issue_S = [&](int j) {          // S_j = Q K_j^T into S buffer j & 1
-        const uint32_t qa = sb + kQOff;
-        const uint32_t ka = slot_addr(2 * j);
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k) {
-          const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-          mma_ss_f8(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 0, 1024), sdesc_sw128(ka + off, 0, 1024),
-                    idS, k > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_PV = [&](int j) {         // O += P_j V_j, P_j over S buffer j & 1
-        const uint32_t va = slot_addr(2 * j + 1);
-        // 32 keys = 32 rows of each 128-channel panel per product; the
-        // panels (channels 0-127, 128-255) are kPanel bytes apart
-#pragma unroll
-        for (int k = 0; k < kBN / 32; ++k)
-          mma_ts_f8(tmem + kColO, tmem + kColS + 128 * (j & 1) + 8 * k, sdesc_sw128(va + 4096 * k, kPanel, 1024),
-                    idO, (j > 0 || k > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar(kQFull), 0, p.ctl, abort_flag);
-      if (ok) ok = kv_wait(0);
-      if (ok) {
-        tc_fence_after();
-        issue_S(0);
-        tc_commit(bar(kSFull + 0));
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        if (j + 1 < n) {
-          // the next scores first; their buffer held P_{j-1}, which the P V
-          // queued in the previous step has read
-          if (!(ok = kv_wait(2 * j + 2))) break;
+      bool ok = true;
+      if (warp == 1) {
+        ok = mbar_wait(bar(kQFull), 0, p.ctl, abort_flag);
+        for (int j = 0; j < n && ok; ++j) {   // S_j = Q K_j^T into S buffer j & 1
+          if (!(ok = kv_wait(2 * j))) break;
+          // the buffer held P_{j-2}: P V_{j-2} must have read it
+          if (j >= 2 && !(ok = mbar_wait(bar(kPVDone + (j & 1)), ((j - 2) >> 1) & 1, p.ctl, abort_flag))) break;
           tc_fence_after();
-          issue_S(j + 1);
-          tc_commit(bar(kSFull + ((j + 1) & 1)));
+          const uint32_t qa = sb + kQOff;
+          const uint32_t ka = slot_addr(2 * j);
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
+            mma_ss_f8(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 0, 1024), sdesc_sw128(ka + off, 0, 1024),
+                      idS, k > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(kSFull + (j & 1)));
+          tc_commit(bar(kKVEmpty + ring_slot(2 * j)));        // K_j read
         }
-        tc_commit(bar(kKVEmpty + ring_slot(2 * j)));          // K_j: read by S_j, queued before
-        if (!(ok = kv_wait(2 * j + 1))) break;
-        if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
-        tc_fence_after();
-        issue_PV(j);
-        tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));      // V_j (and: P V_j is complete)
+      } else {
+        for (int j = 0; j < n && ok; ++j) {   // O += P_j V_j, P_j over S buffer j & 1
+          if (!(ok = kv_wait(2 * j + 1))) break;
+          if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t va = slot_addr(2 * j + 1);
+          // 32 keys = 32 rows of each 128-channel panel per product; the
+          // panels (channels 0-127, 128-255) are kPanel bytes apart
+#pragma unroll
+          for (int k = 0; k < kBN / 32; ++k)
+            mma_ts_f8(tmem + kColO, tmem + kColS + 128 * (j & 1) + 8 * k, sdesc_sw128(va + 4096 * k, kPanel, 1024),
+                      idO, (j > 0 || k > 0) ? 1u : 0u);
+          tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));    // V_j (and: P V_j is complete)
+          tc_commit(bar(kPVDone + (j & 1)));
+        }
+        if (ok) tc_commit(bar(kOFull));
       }
-      if (ok) tc_commit(bar(kOFull));
     }
   } else {
-    // -------------------------------------------------------------- softmax
+    // ------------------------------------------------------- softmax (2-5)
     const int rank = warp & 3;              // tensor-memory lane quarter
     const int r_in_tile = rank * 32 + lane;
     const int row = qbase + r_in_tile;
