@@ -357,3 +357,38 @@ def test_deterministic_beside_a_concurrent_kernel(torch):
         assert fa.fa_get_last_device_status(0) == fa.FA_OK, f"rep {rep}: a wait ran out"
         for x, y in zip((dq, dk, dv), solo):
             assert torch.equal(x.view(torch.int16), y.view(torch.int16)), f"rep {rep}"
+
+
+def test_d64_backward_and_d256_forward_on_two_streams(torch):
+    """The unordered d = 64 backward (two issuing threads) and the d = 256
+    forward (two issuing threads) running at the same time on two streams, each
+    equal to the same call made alone: O, dK and dV bit for bit, dQ within the
+    reordering of its fp32 additions."""
+    w64 = _wl(2, 8, 2048, 2048, 64, True, seed=81)
+    w256 = _wl(1, 8, 2048, 2048, 256, False, seed=82)
+    ins = {}
+    for w in (w64, w256):
+        qb, kb, vb = fa_inputs.make_qkv(w)
+        ins[w.d] = tuple(gu.dev_bf16(x) for x in (qb, kb, vb)) + (gu.dev_bf16(fa_inputs.make_dout(w)),)
+    q, k, v, do = ins[64]
+    o64, lse64 = fa.forward(q, k, v, causal=True)
+    alone_bwd = fa.backward(q, k, v, o64, do, lse64, causal=True)
+    q2, k2, v2, _ = ins[256]
+    alone_fwd, _ = fa.forward(q2, k2, v2)
+    torch.cuda.synchronize()
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(2, 8, 2048, 2048, 64), dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            got_bwd = fa.backward(q, k, v, o64, do, lse64, causal=True, workspace=ws, stream=s1)
+        with torch.cuda.stream(s2):
+            got_fwd, _ = fa.forward(q2, k2, v2, stream=s2)
+        torch.cuda.synchronize()
+        assert fa.fa_get_last_device_status(0) == fa.FA_OK
+        assert torch.equal(got_fwd.view(torch.int16), alone_fwd.view(torch.int16))
+        for name, x, y in zip(("dQ", "dK", "dV"), got_bwd, alone_bwd):
+            if name == "dQ":
+                assert gu.rel_rms(gu.to_f64(x), gu.to_f64(y)) <= 1e-4
+            else:
+                assert torch.equal(x.view(torch.int16), y.view(torch.int16)), name
