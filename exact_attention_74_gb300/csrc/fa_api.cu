@@ -235,10 +235,10 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
   if (st != FA_OK) return st;
   if ((st = check_device_memory({Q, K, V, O, LSE})) != FA_OK) return st;
   const int BH = B * H;
-  const int kv_rows = d == 256 ? 64 : 128;   // rows per K/V box (the d = 256 kernel steps 64 keys)
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
-  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH, kv_rows)) != FA_OK) return st;
-  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH, kv_rows)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH, 128)) != FA_OK) return st;
+  // rows per V box: the d = 256 kernel loads V in 64-key halves
+  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH, d == 256 ? 64 : 128)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmO, O, d, N_q, BH, 32)) != FA_OK) return st;
   a.o = O;
   a.lse = LSE;

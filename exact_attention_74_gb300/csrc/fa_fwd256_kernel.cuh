@@ -3,22 +3,36 @@
 // At d = 256 one query tile's O already takes half of tensor memory (256
 // fp32 columns), so the two-tile ping-pong of the d <= 128 kernel does not
 // fit.  Instead one CTA owns one 128-row query tile and overlaps the work of
-// consecutive key steps of that tile (64 keys per step):
+// consecutive key steps of that tile (128 keys per step):
 //
-//   tensor memory   S_j in one of two 64-column buffers [0,64) / [64,128),
-//                   Q as bf16 pairs [128,256) (copied in once), O [256,512)
-//   warp 0          TMA producer: Q once (64 KB), then K_j, V_j (32 KB each)
-//                   into a ring of five shared-memory slots
-//   warp 1          issues S_{j+1} = Q K_{j+1}^T (A from tensor memory, so only
-//                   K is read from shared memory) as soon as K_{j+1} is in and
-//                   P V_{j-1} has read its buffer, so the tensor core computes
-//                   the next scores while the softmax of the current ones runs
-//   warp 6          issues O += P_j V_j once P_j is written
+//   tensor memory   S_j in one of two 128-column buffers [0,128) / [128,256),
+//                   P_j as bf16 pairs over the first 64 columns of its
+//                   buffer, O [256,512)
+//   shared memory   Q (64 KB, resident) and a ring of five 32 KB slots, each
+//                   holding half a key step: K_j's features 0-127 or
+//                   128-255, V_j's keys 0-63 or 64-127
+//   warp 0          TMA producer: Q once, then the half tiles: K_0, and
+//                   from then on K_{j+1} ahead of V_j
+//   warp 1          issues S_{j+1} = Q K_{j+1}^T (both operands in shared
+//                   memory, N = 128) as soon as each half of K_{j+1} is in
+//                   and P V_{j-1} has read its buffer, so the tensor core
+//                   computes the next scores while the softmax of the
+//                   current ones runs
+//   warp 6          issues O += P_j V_j once P_j is written, half by half
 //   warps 2-5       softmax, one thread per query row (one tensor-memory lane)
 //
-// With one thread issuing both, the next S waited behind that thread's wait
-// for P and its P V products; on threads of their own, each stream goes out
-// as soon as its own inputs are ready.
+// Steps of 128 keys keep every product at the tensor core's full rate
+// (products 64 columns wide run at two thirds of it), and half-tile slots
+// let the next step's K stream in while the current step's products still
+// read the other half: with whole 64 KB tiles in two slots, K_{j+1} could
+// only load after S_j had finished.  The ring holds five halves, so the load
+// order decides what waits: with K_{j+1} queued behind V_j its first half
+// reused the slot of V_{j-1}'s second half and started only when P V_{j-1}
+// had finished, exactly when S_{j+1} needed it; queued ahead of V_j it
+// reuses a slot that P V_{j-2} released a step earlier, and the load
+// latency hides behind the softmax.  With one thread issuing both streams,
+// the next S waited behind that thread's wait for P and its P V products;
+// on threads of their own, each goes out as soon as its inputs are ready.
 //
 // The per-row recurrence is the same online softmax in base 2 with the
 // conditional rescaling of "論文解説: FlashAttention-4 — Algorithm and Kernel
@@ -26,8 +40,7 @@
 // softmaxリスケーリング) as the d <= 128 kernel, including the deferred
 // normalisation by l plus each block's max-element rounding residual.  The
 // rare O rescale must not race with the previous step's P V (queued after
-// S_j), so it first waits for that product's completion, which the release
-// of V_{j-1}'s ring slot signals.
+// S_j), so it first waits for that product's completion barrier.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -41,31 +54,30 @@ namespace fwd256 {
 
 constexpr int D = 256;
 constexpr int kBM = 128;                  // query rows per CTA
-constexpr int kBN = 64;                   // keys per step
+constexpr int kBN = 128;                  // keys per step
 constexpr int kThreads = 224;             // 7 warps
-constexpr int kSlots = 5;                 // K/V ring
+constexpr int kSlots = 5;                 // K/V ring of half tiles
 constexpr int kQPanel = 128 * 128;        // 128 rows x 128 B (64 bf16) swizzle panel
-constexpr int kKPanel = 64 * 128;         // 64 rows x 128 B
+constexpr int kKPanel = 128 * 128;        // K half tile: 2 panels of 128 rows x 128 B
+constexpr int kVPanel = 64 * 128;         // V half tile: 4 panels of 64 rows x 128 B
 constexpr int kQBytes = 4 * kQPanel;      // 64 KB
-constexpr int kSlotBytes = 4 * kKPanel;   // 32 KB
+constexpr int kSlotBytes = 2 * kKPanel;   // 32 KB
 constexpr int kQOff = 0;
 constexpr int kKVOff = kQBytes;
 constexpr int kBarOff = kKVOff + kSlots * kSlotBytes;
 // barrier indices
 constexpr int kQFull = 0;                 // Q tile in shared memory
-constexpr int kQReady = 1;                // Q in tensor memory
-constexpr int kKVFull = 2;                // kSlots
-constexpr int kKVEmpty = 2 + kSlots;      // kSlots
-constexpr int kSFull = 2 + 2 * kSlots;    // 2 (per S buffer)
-constexpr int kPFull = 4 + 2 * kSlots;    // 2 (per S buffer)
-constexpr int kOFull = 6 + 2 * kSlots;
-constexpr int kPVDone = 7 + 2 * kSlots;   // 2 (per S buffer): P V has read the buffer's P
-constexpr int kNumBars = 9 + 2 * kSlots;
+constexpr int kKVFull = 1;                // kSlots
+constexpr int kKVEmpty = 1 + kSlots;      // kSlots
+constexpr int kSFull = 1 + 2 * kSlots;    // 2 (per S buffer)
+constexpr int kPFull = 3 + 2 * kSlots;    // 2 (per S buffer)
+constexpr int kOFull = 5 + 2 * kSlots;
+constexpr int kPVDone = 6 + 2 * kSlots;   // 2 (per S buffer): P V has read the buffer's P
+constexpr int kNumBars = 8 + 2 * kSlots;
 constexpr int kMiscOff = kBarOff + 8 * kNumBars;   // tmem base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + base alignment slack
 // tensor-memory columns
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColQ = 128;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kTmemCols = 512;
 
@@ -74,13 +86,18 @@ struct Params {
   float* lse;
   int BH, N_q, N_kv, causal;
   int n_qtiles;   // ceil(N_q / 128)
-  int n_steps;    // ceil(N_kv / 64)
+  int n_steps;    // ceil(N_kv / 128)
   float c;        // scale * log2(e)
   float tau;      // log2 units
   DevCtl ctl;
 };
 
-// K/V ring: load i is K_{i/2} (even i) or V_{i/2} (odd i).
+// K/V ring of half tiles, in load order: K_0's features 0-127 and 128-255,
+// then per step j < n - 1 the two halves of K_{j+1} followed by V_j's keys
+// 0-63 and 64-127, and last V_{n-1}'s halves.  K_j's half h is load
+// 4j - 2 + h (h for j = 0); V_j's is 4j + 4 + h (4j + 2 + h for the last step).
+__device__ __forceinline__ int k_load(int j, int h) { return j == 0 ? h : 4 * j - 2 + h; }
+__device__ __forceinline__ int v_load(int j, int h, int n) { return (j < n - 1 ? 4 * j + 4 : 4 * j + 2) + h; }
 __device__ __forceinline__ int ring_slot(int i) { return i % kSlots; }
 __device__ __forceinline__ uint32_t ring_phase(int i) { return static_cast<uint32_t>((i / kSlots) & 1); }
 
@@ -121,7 +138,6 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQReady), 4);             // one arrive per softmax warp
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(bar(kKVFull + s), 1);
       mbar_init(bar(kKVEmpty + s), 1);
@@ -153,14 +169,34 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       for (int pn = 0; pn < 4; ++pn)
         tma_load_3d(sb + kQOff + pn * kQPanel, &tmQ, bar(kQFull), pn * 64, qbase, bh);
       const uint64_t keep = l2_policy_evict_last();
-      for (int i = 0; i < 2 * n; ++i) {
+      for (int i = 0; i < 4 * n; ++i) {
         const int s = ring_slot(i);
         if (!mbar_wait(bar(kKVEmpty + s), ring_phase(i) ^ 1, p.ctl, abort_flag)) break;
         const uint32_t dst = sb + kKVOff + s * kSlotBytes;
+        int part, step;   // part: K features 0-127, 128-255; V keys 0-63, 64-127
+        if (i < 2) {
+          part = i;
+          step = 0;
+        } else {
+          const int m = i - 2, blk = m >> 2, r = m & 3;
+          if (blk < n - 1) {
+            part = r;
+            step = r < 2 ? blk + 1 : blk;
+          } else {
+            part = 2 + r;
+            step = blk;
+          }
+        }
+        const int key0 = step * kBN;
         mbar_arrive_expect_tx(bar(kKVFull + s), kSlotBytes);
-        for (int pn = 0; pn < 4; ++pn)
-          tma_load_3d_hint(dst + pn * kKPanel, (i & 1) ? &tmV : &tmK, bar(kKVFull + s), pn * 64,
-                           (i >> 1) * kBN, bh, keep);
+        if (part < 2) {
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_3d_hint(dst + pn * kKPanel, &tmK, bar(kKVFull + s), (2 * part + pn) * 64, key0, bh, keep);
+        } else {
+          for (int pn = 0; pn < 4; ++pn)
+            tma_load_3d_hint(dst + pn * kVPanel, &tmV, bar(kKVFull + s), pn * 64, key0 + 64 * (part - 2), bh,
+                             keep);
+        }
       }
     }
   } else if (warp == 1 || warp == 6) {
@@ -172,32 +208,41 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       auto kv_wait = [&](int i) { return mbar_wait(bar(kKVFull + ring_slot(i)), ring_phase(i), p.ctl, abort_flag); };
       bool ok = true;
       if (warp == 1) {
-        ok = mbar_wait(bar(kQReady), 0, p.ctl, abort_flag);
+        ok = mbar_wait(bar(kQFull), 0, p.ctl, abort_flag);
         for (int j = 0; j < n && ok; ++j) {   // S_j = Q K_j^T into S buffer j & 1
-          if (!(ok = kv_wait(2 * j))) break;
           // the buffer held P_{j-2}: P V_{j-2} must have read it
           if (j >= 2 && !(ok = mbar_wait(bar(kPVDone + (j & 1)), ((j - 2) >> 1) & 1, p.ctl, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t ka = slot_addr(2 * j);
+          for (int h = 0; h < 2; ++h) {       // feature halves of K_j, one ring slot each
+            const int ik = k_load(j, h);
+            if (!(ok = kv_wait(ik))) break;
+            tc_fence_after();
+            const uint32_t ka = slot_addr(ik);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ts(tmem + kColS + 64 * (j & 1), tmem + kColQ + 8 * k,
-                   sdesc_sw128(ka + (k >> 2) * kKPanel + (k & 3) * 32, 0, 1024), idS, k > 0 ? 1u : 0u);
-          tc_commit(bar(kSFull + (j & 1)));
-          tc_commit(bar(kKVEmpty + ring_slot(2 * j)));        // K_j read
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t qa = sb + kQOff + (2 * h + (k >> 2)) * kQPanel + (k & 3) * 32;
+              const uint32_t kb = ka + (k >> 2) * kKPanel + (k & 3) * 32;
+              mma_ss(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa, 0, 1024), sdesc_sw128(kb, 0, 1024), idS,
+                     (h > 0 || k > 0) ? 1u : 0u);
+            }
+            if (h == 1) tc_commit(bar(kSFull + (j & 1)));
+            tc_commit(bar(kKVEmpty + ring_slot(ik)));   // this half of K_j read
+          }
         }
       } else {
         for (int j = 0; j < n && ok; ++j) {   // O += P_j V_j, P_j over S buffer j & 1
-          if (!(ok = kv_wait(2 * j + 1))) break;
           if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t va = slot_addr(2 * j + 1);
+          for (int h = 0; h < 2; ++h) {       // key halves of V_j, one ring slot each
+            const int iv = v_load(j, h, n);
+            if (!(ok = kv_wait(iv))) break;
+            tc_fence_after();
+            const uint32_t va = slot_addr(iv);
 #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            mma_ts(tmem + kColO, tmem + kColS + 64 * (j & 1) + 8 * k, sdesc_sw128(va + k * 2048, kKPanel, 1024),
-                   idO, (j > 0 || k > 0) ? 1u : 0u);
-          tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));    // V_j (and: P V_j is complete)
-          tc_commit(bar(kPVDone + (j & 1)));
+            for (int k = 0; k < 4; ++k)
+              mma_ts(tmem + kColO, tmem + kColS + 128 * (j & 1) + 32 * h + 8 * k,
+                     sdesc_sw128(va + k * 2048, kVPanel, 1024), idO, (j > 0 || h > 0 || k > 0) ? 1u : 0u);
+            tc_commit(bar(kKVEmpty + ring_slot(iv)));   // this half of V_j read
+          }
+          if (ok) tc_commit(bar(kPVDone + (j & 1)));   // P V_j complete
         }
         if (ok) tc_commit(bar(kOFull));
       }
@@ -210,30 +255,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t lane_addr = static_cast<uint32_t>(rank * 32) << 16;
     const uint32_t tO = tmem + lane_addr + kColO;
     const float c = p.c;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kQFull), 0, p.ctl, abort_flag));
-    if (ok) {
-      // Q row into tensor memory as bf16 pairs (column w holds d = 2w, 2w+1),
-      // read from TMA's 128-byte swizzled panels (chunk c at c ^ (row & 7)).
-      uint32_t qa[64], qb[64];
-#pragma unroll
-      for (int pn = 0; pn < 4; ++pn) {
-        const uint8_t* rp = smem + kQOff + pn * kQPanel + r_in_tile * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rp + ((ch ^ (r_in_tile & 7)) * 16));
-          uint32_t* dst = (pn < 2 ? qa : qb) + (pn & 1) * 32 + ch * 4;
-          dst[0] = w.x;
-          dst[1] = w.y;
-          dst[2] = w.z;
-          dst[3] = w.w;
-        }
-      }
-      tmem_st_x64(tmem + lane_addr + kColQ, qa);
-      tmem_st_x64(tmem + lane_addr + kColQ + 64, qb);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kQReady));
-    }
+    bool ok = true;
     float m_ref = -INFINITY;
     float l = 0.f;      // sum of the fp32 probabilities: gives the LSE
     float lr = 0.f;     // rounding residuals of the blocks' largest P
@@ -243,18 +265,18 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + b), (j >> 1) & 1, p.ctl, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem + lane_addr + kColS + 64 * b;
-      uint32_t s[64];
-      tmem_ld_x64(tS, s);
+      const uint32_t tS = tmem + lane_addr + kColS + 128 * b;
+      uint32_t s[128];
+      tmem_ld_x128(tS, s);
       const int lim = key_lim - j * kBN;
       if (__any_sync(0xffffffffu, lim < kBN - 1)) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = __float_as_uint(-INFINITY);
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 64; i += 8) {
+      for (int i = 0; i < 128; i += 8) {
         mx[0] = max3(mx[0], __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
         mx[1] = max3(mx[1], __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
         mx[2] = max3(mx[2], __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
@@ -275,10 +297,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         m_ref = m_new;
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // P_{j-1} V_{j-1} may still be accumulating into O: wait for it (the
-        // release of V_{j-1}'s slot is committed after it)
-        const int iv = 2 * j - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVEmpty + ring_slot(iv)), ring_phase(iv), p.ctl, abort_flag));
+        // P_{j-1} V_{j-1} may still be accumulating into O: wait for it
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, p.ctl, abort_flag));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
@@ -299,9 +319,9 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const float2 neg2 = make_float2(-m_ref, -m_ref);
       float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       float pmax = 0.f;   // largest P as computed (emulated exponentials differ slightly)
-      uint32_t pk[32];
+      uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 64; ++i) {
         const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
         const float e0 = ex2_mix<EMU>(x.x, 2 * i);
         const float e1 = ex2_mix<EMU>(x.y, 2 * i + 1);
@@ -309,7 +329,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if constexpr (EMU > 0) pmax = max3(pmax, e0, e1);
         pk[i] = pack_bf16x2(e0, e1);
       }
-      tmem_st_x32(tS, pk);   // waits for its own stores
+      tmem_st_x64(tS, pk);   // waits for its own stores
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kPFull + b));
