@@ -263,8 +263,8 @@ def event_times(torch, stream, fn, reps, warmup=3):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-_KERNELS = ("fwd_kernel", "fwd256_kernel", "prep_kernel", "main_kernel", "convert_kernel", "fwd8_kernel",
-            "fwd8_256_kernel", "quant_qk_kernel", "quant_v_kernel")
+_KERNELS = ("fwd_kernel", "fwd64_kernel", "fwd256p_kernel", "prep_kernel", "main_kernel", "main64_kernel",
+            "pair_kernel", "convert_kernel", "fwd8_kernel", "fwd8_256_kernel", "quant_qk_kernel", "quant_v_kernel")
 
 
 def _short_kernel_name(name: str) -> str:

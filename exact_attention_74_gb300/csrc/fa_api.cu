@@ -236,9 +236,9 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
   if ((st = check_device_memory({Q, K, V, O, LSE})) != FA_OK) return st;
   const int BH = B * H;
   if ((st = make_map_bf16(&a.tmQ, Q, d, N_q, BH)) != FA_OK) return st;
-  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH, 128)) != FA_OK) return st;
-  // rows per V box: the d = 256 kernel loads V in 64-key halves
-  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH, d == 256 ? 64 : 128)) != FA_OK) return st;
+  // rows per K box: at d = 256 each CTA of a pair loads 64 keys of a step
+  if ((st = make_map_bf16(&a.tmK, K, d, N_kv, BH, d == 256 ? 64 : 128)) != FA_OK) return st;
+  if ((st = make_map_bf16(&a.tmV, V, d, N_kv, BH, 128)) != FA_OK) return st;
   if ((st = make_map_bf16(&a.tmO, O, d, N_q, BH, 32)) != FA_OK) return st;
   a.o = O;
   a.lse = LSE;

@@ -25,7 +25,7 @@ struct FwdLaunch {
 
 cudaError_t launch_fwd_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_d128(const FwdLaunch& a);
-cudaError_t launch_fwd_d256(const FwdLaunch& a);   // 64-row K/V boxes
+cudaError_t launch_fwd_d256(const FwdLaunch& a);   // 64-row K boxes, pairs of CTAs
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO;   // same map shape as the forward's
