@@ -100,6 +100,15 @@ def test_ragged_rectangular(torch, d, causal, nq, nkv):
     full_compare(torch, _wl(2, 1, nq, nkv, d, causal, seed=nq + nkv))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nkv", [(401, 401), (129, 515), (515, 129), (897, 640)])
+def test_query_tile_pairs_across_heads_d256(torch, causal, nq, nkv):
+    """d = 256 runs on pairs of CTAs, one pair per two 128-row query tiles of
+    a (batch, head): 15 heads with an odd or even number of query tiles and
+    ragged key tails, every element compared."""
+    full_compare(torch, _wl(3, 5, nq, nkv, 256, causal, seed=nq * 3 + nkv))
+
+
 @pytest.mark.parametrize("emu", [0, 8, 16])
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
