@@ -11,23 +11,26 @@
 //                   (P_j, four e4m3 per column, over its first 32 columns),
 //                   O [256,512)
 //   warp 0          TMA producer: the Q codes once (32 KB), then K_j, V_j
-//                   (32 KB each: two 128-byte panels) into a five-slot ring
-//   warp 1          issues S_{j+1} = Q K_{j+1}^T (both operands in shared
-//                   memory, eight kind::f8f6f4 products of K = 32) as soon as
-//                   K_{j+1} is in and P V_{j-1} has read its buffer, so the
-//                   tensor core computes the next scores while the softmax of
-//                   the current ones runs
-//   warp 6          issues O += P_j V_j (four products of N = 256, V as the
-//                   MN-major operand) once P_j is written; on one thread the
-//                   next S would wait behind the wait for P_j
+//                   (32 KB each: two 128-byte panels) into a five-slot ring,
+//                   K_0 first and then K_{j+1} ahead of V_j
+//   warps 1, 6      issuing threads of the even and the odd key steps: each
+//                   issues O += P_j V_j (four kind::f8f6f4 products of
+//                   N = 256, V as the MN-major operand) once P_j is written,
+//                   followed by S_{j+2} = Q K_{j+2}^T (eight products of
+//                   K = 32, both operands in shared memory) into the buffer
+//                   P_j occupies
 //   warps 2-5       softmax, one thread per query row: S_j scaled by
 //                   c = scale log2(e) / (inv_q inv_k_j), the online softmax
 //                   with conditional rescaling, P rounded to e4m3
 //
-// The rare O rescale must not race with the previous step's P V (queued
-// after S_j), so it first waits for that product's completion, which the
-// release of V_{j-1}'s ring slot signals.  O is divided by (l + residuals)
-// inv_v at the end, as in the d = 128 kernel.
+// The tensor core runs one thread's products in order, so S_{j+2} follows
+// P V_j without waiting for its completion; the two threads keep each
+// other's waits off the tensor core's queue.  P V_j goes into the queue after
+// P V_{j-1} (an issue barrier between the threads, not a completion wait):
+// P V_0 initialises O, and a fixed order keeps the sums reproducible.  The
+// rare O rescale must not race with the previous step's P V, so it first
+// waits for that product's completion barrier.  O is divided by
+// (l + residuals) inv_v at the end, as in the d = 128 kernel.
 #pragma once
 
 #include "fa_fwd8_kernel.cuh"
@@ -53,7 +56,8 @@ constexpr int kSFull = 1 + 2 * kSlots;    // 2 (per S buffer)
 constexpr int kPFull = 3 + 2 * kSlots;    // 2 (per S buffer)
 constexpr int kOFull = 5 + 2 * kSlots;
 constexpr int kPVDone = 6 + 2 * kSlots;   // 2 (per S buffer): P V has read the buffer's P
-constexpr int kNumBars = 8 + 2 * kSlots;
+constexpr int kPVIssued = 8 + 2 * kSlots; // P V_j issued (orders P V_{j+1} after it)
+constexpr int kNumBars = 9 + 2 * kSlots;
 constexpr int kMiscOff = kBarOff + 8 * kNumBars;   // tmem base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + base alignment slack
 // tensor-memory columns
@@ -75,7 +79,9 @@ struct Params {
   DevCtl ctl;
 };
 
-// K/V ring: load i is K_{i/2} (even i) or V_{i/2} (odd i).
+// K/V ring in load order: K_0, then K_{j+1} ahead of V_j, and V_{n-1} last.
+__device__ __forceinline__ int k_load(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int v_load(int j, int n) { return j < n - 1 ? 2 * j + 2 : 2 * n - 1; }
 __device__ __forceinline__ int ring_slot(int i) { return i % kSlots; }
 __device__ __forceinline__ uint32_t ring_phase(int i) { return static_cast<uint32_t>((i / kSlots) & 1); }
 
@@ -120,6 +126,7 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(bar(kOFull), 1);
     mbar_init(bar(kPVDone + 0), 1);
     mbar_init(bar(kPVDone + 1), 1);
+    mbar_init(bar(kPVIssued), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -143,55 +150,68 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int i = 0; i < 2 * n; ++i) {
         const int s = ring_slot(i);
         if (!mbar_wait(bar(kKVEmpty + s), ring_phase(i) ^ 1, p.ctl, abort_flag)) break;
+        bool is_k;
+        int step;
+        if (i == 0) {
+          is_k = true;
+          step = 0;
+        } else {
+          const int m = i - 1, blk = m >> 1;
+          is_k = blk < n - 1 && (m & 1) == 0;
+          step = is_k ? blk + 1 : blk;
+        }
         const uint32_t dst = sb + kKVOff + s * kTileBytes;
         mbar_arrive_expect_tx(bar(kKVFull + s), kTileBytes);
         for (int pn = 0; pn < 2; ++pn)       // channels 128 pn .. 128 pn + 127 of 128 keys
-          tma_load_3d_hint(dst + pn * kPanel, (i & 1) ? &tmV : &tmK, bar(kKVFull + s), pn * 128,
-                           (i >> 1) * kBN, bh, keep);
+          tma_load_3d_hint(dst + pn * kPanel, is_k ? &tmK : &tmV, bar(kKVFull + s), pn * 128, step * kBN, bh, keep);
       }
     }
   } else if (warp == 1 || warp == 6) {
-    // ---------------------------------------------- MMA issuers (S; P V)
+    // ------------------------------- MMA issuers: steps j of parity par
     if (lane == 0) {
+      const int par = warp == 1 ? 0 : 1;
       constexpr uint32_t idS = idesc_e4m3(kBM, kBN);            // S = Q K^T, both K-major
       constexpr uint32_t idO = idesc_e4m3(kBM, D, true);        // O += P V, V MN-major
       auto slot_addr = [&](int i) { return sb + kKVOff + ring_slot(i) * kTileBytes; };
       auto kv_wait = [&](int i) { return mbar_wait(bar(kKVFull + ring_slot(i)), ring_phase(i), p.ctl, abort_flag); };
-      bool ok = true;
-      if (warp == 1) {
-        ok = mbar_wait(bar(kQFull), 0, p.ctl, abort_flag);
-        for (int j = 0; j < n && ok; ++j) {   // S_j = Q K_j^T into S buffer j & 1
-          if (!(ok = kv_wait(2 * j))) break;
-          // the buffer held P_{j-2}: P V_{j-2} must have read it
-          if (j >= 2 && !(ok = mbar_wait(bar(kPVDone + (j & 1)), ((j - 2) >> 1) & 1, p.ctl, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t qa = sb + kQOff;
-          const uint32_t ka = slot_addr(2 * j);
+      auto issue_S = [&](int j) -> bool {   // S_j = Q K_j^T into S buffer j & 1
+        const int ik = k_load(j);
+        if (!kv_wait(ik)) return false;
+        tc_fence_after();
+        const uint32_t qa = sb + kQOff;
+        const uint32_t ka = slot_addr(ik);
 #pragma unroll
-          for (int k = 0; k < D / 32; ++k) {
-            const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-            mma_ss_f8(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 0, 1024), sdesc_sw128(ka + off, 0, 1024),
-                      idS, k > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(kSFull + (j & 1)));
-          tc_commit(bar(kKVEmpty + ring_slot(2 * j)));        // K_j read
+        for (int k = 0; k < D / 32; ++k) {
+          const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
+          mma_ss_f8(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 0, 1024), sdesc_sw128(ka + off, 0, 1024),
+                    idS, k > 0 ? 1u : 0u);
         }
-      } else {
-        for (int j = 0; j < n && ok; ++j) {   // O += P_j V_j, P_j over S buffer j & 1
-          if (!(ok = kv_wait(2 * j + 1))) break;
-          if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t va = slot_addr(2 * j + 1);
-          // 32 keys = 32 rows of each 128-channel panel per product; the
-          // panels (channels 0-127, 128-255) are kPanel bytes apart
+        tc_commit(bar(kSFull + (j & 1)));
+        tc_commit(bar(kKVEmpty + ring_slot(ik)));        // K_j read
+        return true;
+      };
+      bool ok = mbar_wait(bar(kQFull), 0, p.ctl, abort_flag);
+      if (ok && par < n) ok = issue_S(par);
+      for (int j = par; j < n && ok; j += 2) {   // O += P_j V_j, P_j over S buffer j & 1
+        if (!(ok = mbar_wait(bar(kPFull + (j & 1)), (j >> 1) & 1, p.ctl, abort_flag))) break;
+        const int iv = v_load(j, n);
+        if (!(ok = kv_wait(iv))) break;
+        // the other thread's P V_{j-1} goes into the tensor core's queue first
+        if (j >= 1 && !(ok = mbar_wait(bar(kPVIssued), (j - 1) & 1, p.ctl, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t va = slot_addr(iv);
 #pragma unroll
-          for (int k = 0; k < kBN / 32; ++k)
-            mma_ts_f8(tmem + kColO, tmem + kColS + 128 * (j & 1) + 8 * k, sdesc_sw128(va + 4096 * k, kPanel, 1024),
-                      idO, (j > 0 || k > 0) ? 1u : 0u);
-          tc_commit(bar(kKVEmpty + ring_slot(2 * j + 1)));    // V_j (and: P V_j is complete)
-          tc_commit(bar(kPVDone + (j & 1)));
-        }
-        if (ok) tc_commit(bar(kOFull));
+        for (int k = 0; k < kBN / 32; ++k)
+          mma_ts_f8(tmem + kColO, tmem + kColS + 128 * (j & 1) + 8 * k, sdesc_sw128(va + 4096 * k, kPanel, 1024),
+                    idO, (j > 0 || k > 0) ? 1u : 0u);
+        tc_fence_before();
+        mbar_arrive(bar(kPVIssued));
+        tc_commit(bar(kKVEmpty + ring_slot(iv)));    // V_j read
+        tc_commit(bar(kPVDone + (j & 1)));           // (and every earlier P V complete)
+        if (j == n - 1) tc_commit(bar(kOFull));
+        // S_{j+2} overwrites P_j: issued after P V_j by the same thread, the
+        // tensor core runs it after P V_j has read its operand
+        if (j + 2 < n) ok = issue_S(j + 2);
       }
     }
   } else {
@@ -248,10 +268,8 @@ fwd8_256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         m_ref = m_new;
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // P_{j-1} V_{j-1} may still be accumulating into O: wait for it (the
-        // release of V_{j-1}'s slot is committed after it)
-        const int iv = 2 * j - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVEmpty + ring_slot(iv)), ring_phase(iv), p.ctl, abort_flag));
+        // P_{j-1} V_{j-1} may still be accumulating into O: wait for it
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kPVDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, p.ctl, abort_flag));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
