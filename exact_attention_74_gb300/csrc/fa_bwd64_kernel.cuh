@@ -19,13 +19,18 @@
 //   warp 1   S_{i+1}  as soon as the compute warps have read S_i,
 //            dV_i     once P_i is written (and dO_i has landed),
 //            dK_i     once dS_i is in shared memory;
-//   warp 10  dP_{i+1} as soon as the compute warps have read dP_i,
+//   warp 18  dP_{i+1} as soon as the compute warps have read dP_i,
 //            dQ_i     once dS_i is in shared memory and dQ_{i-1} has left
 //                     dQ's columns,
-// so the compute warps find the next S and dP complete when they reach them;
-// they drain dQ_{i-1} right after handing P_i over, through a dedicated box
-// area (the drain does not wait for a dead Q/dO buffer), and they rewrite dS
-// and the producer refills a Q/dO stage only once both threads' products of
+// so the compute warps find the next S and dP complete when they reach them.
+// Sixteen compute warps (2-17), four per tensor-memory lane quarter, each
+// take 32 of a tile's 128 query columns of P and dS: at d = 64 a step's
+// element work is as large as at d = 128 while its products are half, and
+// 32 columns per thread keep the warps within the registers that 19 warps
+// leave each (96); warps 2-9 also drain dQ and write dK and dV.  They
+// drain dQ_{i-1} right after handing P_i over, through a dedicated box
+// area (the drain does not wait for a dead Q/dO buffer); the compute warps
+// rewrite dS and the producer refills a Q/dO stage only once both threads' products of
 // that tile have completed (per-stage barriers, so no wait can be mistaken
 // for the same stage's next phase).
 // "FlashAttention: GPUメモリ階層を活用したアテンション最適化の分析" §7.2
@@ -42,7 +47,7 @@ namespace bwd64 {
 constexpr int D = 64;
 constexpr int kBM = 128;          // keys per CTA
 constexpr int kBN = 128;          // queries per step
-constexpr int kThreads = 352;     // warps 0-10
+constexpr int kThreads = 608;     // warps 0-18
 constexpr int kTile = 128 * D * 2;                      // 16 KB
 constexpr int kPanel = 128 * 128;                       // 128 rows x 128 B
 constexpr int kK = 0;
@@ -55,7 +60,7 @@ constexpr int kBar = kDrain + 8 * 4096;
 enum : int {
   bKV = 0, bQ = 1, bDO = 3,                             // two of bQ and bDO (per stage)
   bS = 5, bSFree, bP, bPFree, bDP, bDPFree, bDS, bDQFree, bAcc,
-  bDQ = 14, bKD = 16,                                   // per stage: dQ_i (warp 10), dK_i (warp 1) complete
+  bDQ = 14, bKD = 16,                                   // per stage: dQ_i (warp 18), dK_i (warp 1) complete
   kNumBars = 18
 };
 constexpr int kMisc = kBar + 8 * kNumBars;
@@ -64,7 +69,8 @@ static_assert(kSmem <= 232448, "shared memory");
 static_assert(kStageBytes % 1024 == 0 && kDS % 1024 == 0 && kDrain % 1024 == 0, "alignment");
 constexpr uint32_t kColS = 0, kColP = 128, kColDP = 192, kColDQ = 320, kColDV = 384, kColDK = 448;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kWarps = 8;    // compute warps: one arrival each
+constexpr uint32_t kWarps = 16;   // compute warps: one arrival each
+constexpr uint32_t kDrainWarps = 8;   // of them, those that drain dQ and write dK, dV
 
 __global__ void __launch_bounds__(kThreads, 1)
 main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -107,7 +113,7 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(bar(bP), kWarps);
     mbar_init(bar(bDPFree), kWarps);
     mbar_init(bar(bDS), kWarps);
-    mbar_init(bar(bDQFree), kWarps);
+    mbar_init(bar(bDQFree), kDrainWarps);
     *abort_flag = 0;
     mbar_init_fence();
     *logical_slot = b;
@@ -158,7 +164,7 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
     }
-  } else if (n_it > 0 && (warp == 1 || warp == 10)) {
+  } else if (n_it > 0 && (warp == 1 || warp == 18)) {
     // ------------------------------------------------------- MMA issuers
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
@@ -245,10 +251,12 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
     }
-  } else if (warp >= 2 && warp <= 9) {
+  } else if (warp >= 2 && warp <= 17) {
     // ------------------------------------------------ P and dS, dQ drainage
     const int quad = warp & 3;               // tensor-memory lane quarter
-    const int half = (warp - 2) >> 2;        // query columns [64 half, 64 half + 64)
+    const int part = (warp - 2) >> 2;        // query columns [32 part, 32 part + 32)
+    const bool drainer = part < 2;           // warps 2-9 also drain dQ and write dK, dV
+    const int half = part & 1;               // their half of dQ's (and dK's, dV's) columns
     const int r = quad * 32 + lane;          // key row within the tile (and dQ query row)
     const int kg = j * kBM + r;              // global key index
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
@@ -295,16 +303,16 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int lim = (p.causal && i == j) ? r : 0;
       const bool masked = __any_sync(0xffffffffu, lim > 0 || !key_ok);
       // ---- P = 2^(S c - LSE log2 e)
-      float pf[2][32];
-      uint32_t pk[2][16];
+      float pf[1][32];
+      uint32_t pk[1][16];
       {
-        uint32_t sv[64];
-        tmem_ld_x64(tmem + lane_addr + kColS + 64 * half, sv);
+        uint32_t sv[32];
+        tmem_ld_x32(tmem + lane_addr + kColS + 32 * part, sv);
         tc_fence_before();
         signal(bSFree);                     // the next S may be written now
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int ch = 2 * half + cc;        // 32-query chunk
+        for (int cc = 0; cc < 1; ++cc) {
+          const int ch = part;                 // 32-query chunk
 #pragma unroll
           for (int u = 0; u < 32; u += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * ch + u);
@@ -332,8 +340,7 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (!ok) break;
         tc_fence_after();
       }
-      tmem_st_x16(tmem + lane_addr + kColP + 32 * half, pk[0]);
-      tmem_st_x16(tmem + lane_addr + kColP + 32 * half + 16, pk[1]);
+      tmem_st_x16(tmem + lane_addr + kColP + 16 * part, pk[0]);
       tc_fence_before();
       signal(bP);                           // dV may use P_i now
       if (it > 0) {                         // dQ_{i-1} (dK_{i-1} too: dS may be rewritten)
@@ -341,19 +348,19 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         ok = __all_sync(0xffffffffu, wait(bDQ + sp, (it - 1) >> 1) && wait(bKD + sp, (it - 1) >> 1));
         if (!ok) break;
         tc_fence_after();
-        drain(it - 1, true);
+        if (drainer) drain(it - 1, true);
       }
       // ---- dS = P o (dP - D)
       ok = __all_sync(0xffffffffu, wait(bDP, it));
       if (!ok) break;
       tc_fence_after();
-      uint32_t dpv[64];
-      tmem_ld_x64(tmem + lane_addr + kColDP + 64 * half, dpv);
+      uint32_t dpv[32];
+      tmem_ld_x32(tmem + lane_addr + kColDP + 32 * part, dpv);
       tc_fence_before();
       signal(bDPFree);                      // the next dP may be written now
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int ch = 2 * half + cc;
+      for (int cc = 0; cc < 1; ++cc) {
+        const int ch = part;
         uint32_t dk[16];
         const uint32_t* dp = dpv + 32 * cc;
 #pragma unroll
@@ -379,7 +386,7 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       fence_async_smem();
       signal(bDS);                          // dQ and dK may read dS now
     }
-    if (ok && n_it > 0) {                   // the last tile's partial dQ
+    if (ok && n_it > 0 && drainer) {        // the last tile's partial dQ
       ok = __all_sync(0xffffffffu, wait(bDQ + ((n_it - 1) & 1), (n_it - 1) >> 1));
       if (ok) {
         tc_fence_after();
@@ -387,10 +394,10 @@ main64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
     }
     // ----------------------------------------------------- dK, dV epilogue
-    bool ready = ok;
+    bool ready = ok && drainer;
     if (n_it > 0 && ready) ready = wait(bAcc, 0);
     ready = __all_sync(0xffffffffu, ready);
-    if (n_it == 0 || ready) {
+    if (drainer && (n_it == 0 || ready)) {
       if (n_it > 0) tc_fence_after();
       constexpr int kCpr = D / 16;                // 16-byte chunks per row slice
       constexpr int kRowsPerStore = 32 / kCpr;
