@@ -20,7 +20,7 @@ __all__ = [
     "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FAError", "library", "library_path",
     "fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "forward_fp8", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_last_device_status",
     "fa_bwd_noalloc", "FA_BWD_NOALLOC_MAX_WORKSPACE", "fa_bwd_ex", "fa_bwd_pair",
-    "fa_set_wait_timeout_ns", "fa_status_string", "fa_test_exp2", "fa_test_mma_tile",
+    "fa_set_wait_timeout_ns", "fa_status_string", "fa_test_exp2", "fa_test_mma_tile", "fa_test_mma_pair",
     "fa_test_mma_fp8", "fa_test_wait_timeout", "forward", "backward", "EXPORTED_SYMBOLS",
 ]
 
@@ -54,6 +54,7 @@ _SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_test_exp2": (_i, [_vp, _vp, _ll, _i, _vp]),
     "fa_test_mma_tile": (_i, [_vp, _vp, _vp, _i, _i, _vp]),
+    "fa_test_mma_pair": (_i, [_vp, _vp, _vp, _i, _i, _vp]),
     "fa_test_mma_fp8": (_i, [_vp, _vp, _vp, _vp, _i, _vp]),
     "fa_test_wait_timeout": (_i, [_ull, _vp]),
 }
@@ -163,6 +164,10 @@ def fa_test_exp2(x, y, n, mode, stream=0):
 
 def fa_test_mma_tile(A, B, C, K, mode, stream=0):
     return _call("fa_test_mma_tile", A, B, C, K, mode, stream)
+
+
+def fa_test_mma_pair(A, B, C, K, mode, stream=0):
+    return _call("fa_test_mma_pair", A, B, C, K, mode, stream)
 
 
 def fa_test_mma_fp8(A, B, C, A_codes, mode, stream=0):

@@ -7,6 +7,7 @@
 #include "fa_internal.h"
 #include "fa_testing.h"
 #include "ptx.cuh"
+#include "ptx_pair.cuh"
 
 namespace fa {
 namespace testing {
@@ -115,6 +116,108 @@ mma_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
+  }
+}
+
+// One 256 x 128 x K product of a CTA pair (cta_group::2).  Shared memory of
+// each CTA: its A rows (K/64 panels of 128 rows), its half of B (K-major:
+// K/64 panels of 64 rows; N-major: one 64-column panel of K rows), two
+// barriers, the tensor-memory base and the abort flag.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTileThreads, 1)
+mma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __nv_bfloat16* A, float* Cout, int K, int mode, DevCtl ctl) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {   // the same offset in both CTAs, so both return here or neither does
+    if (threadIdx.x == 0) atomicOr(ctl.status, kStatusLaunchConfig);
+    return;
+  }
+  const int a_bytes = 128 * K * 2, b_bytes = 64 * K * 2;
+  const uint32_t sA = sb, sB = sb + a_bytes;
+  const uint32_t bar_full = sb + a_bytes + b_bytes, bar_done = bar_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + a_bytes + b_bytes + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + a_bytes + b_bytes + 20);
+  const bool b_mn = mode & 1, a_tmem = mode & 2;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const uint32_t peer_abort = map_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+  const int warp = threadIdx.x >> 5;
+  auto wait = [&](uint32_t b, uint32_t parity) { return pair_wait(b, parity, ctl, abort_flag, peer_abort); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_full, leader ? 2 : 1);   // the leader also counts CTA 1's forwarded arrival
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc_pair(smem_u32(tmem_slot), 256);
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int r = static_cast<int>(rank);
+
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar_full, (a_tmem ? 0 : a_bytes) + b_bytes);
+    for (int pn = 0; pn < K / 64 && !a_tmem; ++pn)
+      tma_load_3d(sA + pn * 16384, &tmA, bar_full, pn * 64, 128 * r, 0);
+    if (!b_mn) {
+      for (int pn = 0; pn < K / 64; ++pn) tma_load_3d(sB + pn * 8192, &tmB, bar_full, pn * 64, 64 * r, 0);
+    } else {
+      tma_load_3d(sB, &tmB, bar_full, 64 * r, 0, 0);   // columns 64 r .. 64 r + 63 of [K, 128], K rows
+    }
+  }
+  if (a_tmem) {
+    // thread t writes row 128 r + t of A into tensor-memory lane t, columns
+    // 128.. as packed bf16 pairs (low half = even k)
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(A + static_cast<size_t>(128 * r + threadIdx.x) * K);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    for (int ch = 0; ch < K / 32; ++ch) {
+      uint32_t v[16];
+      for (int i = 0; i < 16; ++i) v[i] = arow[ch * 16 + i];
+      tmem_st_x16(tmem + lane_addr + 128 + 16 * ch, v);
+    }
+    tc_fence_before();
+  }
+  __syncwarp();
+  __syncthreads();
+  if (threadIdx.x == 0 && !leader) {
+    // this CTA's operands are in place: count them on the leader's barrier
+    if (wait(bar_full, 0)) mbar_arrive_remote_relaxed(map_shared(bar_full, 0));
+  }
+  if (threadIdx.x == 0 && leader) {
+    if (wait(bar_full, 0)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(256, 128, false, b_mn);
+      for (int k = 0; k < K / 16; ++k) {
+        const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, K * 128, 1024)
+                                 : sdesc_sw128(sB + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024);
+        if (a_tmem)
+          mma_ts_pair(tmem, tmem + 128 + 8 * k, bd, idesc, k > 0);
+        else
+          mma_ss_pair(tmem, sdesc_sw128(sA + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024), bd, idesc, k > 0);
+      }
+      tc_commit_pair(bar_done, 3);   // both CTAs
+    }
+  }
+  __syncwarp();
+  if (__all_sync(0xffffffffu, wait(bar_done, 0))) {
+    tc_fence_after();
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    float* crow = Cout + static_cast<size_t>(128 * r + threadIdx.x) * 128;
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t v[32];
+      tmem_ld_x32(tmem + lane_addr + 32 * ch, v);
+      for (int i = 0; i < 32; ++i) crow[32 * ch + i] = __uint_as_float(v[i]);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();   // neither CTA leaves while the other may still use its memory
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 256);
   }
 }
 
@@ -251,6 +354,31 @@ int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode, fa
     return FA_ERR_CUDA;
   }
   kern<<<1, testing::kTileThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      tmA, tmB, static_cast<const __nv_bfloat16*>(A), C, K, mode, ctl);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_test_mma_pair(const void* A, const void* B, float* C, int K, int mode, fa_stream_t stream) {
+  if (!A || !B || !C || (K != 64 && K != 128) || mode < 0 || mode > 3) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) % 16)
+    return FA_ERR_ALIGN;
+  DevCtl ctl;
+  int st = device_ctl(&ctl);
+  if (st != FA_OK) return st;
+  CUtensorMap tmA, tmB;
+  if ((st = make_map_bf16(&tmA, A, K, 256, 1)) != FA_OK) return st;          // [256, K]: 128-row boxes
+  if (mode & 1)
+    st = make_map_bf16(&tmB, B, 128, K, 1, K);   // [K, 128]: 64-column boxes of K rows
+  else
+    st = make_map_bf16(&tmB, B, K, 128, 1, 64);  // [128, K]: 64-row boxes
+  if (st != FA_OK) return st;
+  const int smem = 128 * K * 2 + 64 * K * 2 + 64;
+  auto kern = testing::mma_pair_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  kern<<<2, testing::kTileThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       tmA, tmB, static_cast<const __nv_bfloat16*>(A), C, K, mode, ctl);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -52,6 +52,25 @@ int fa_test_mma_tile(const void* A, const void* B, float* C, int K, int mode,
                      fa_stream_t stream);
 
 /*
+ * fa_test_mma_pair -- C = A * B^T (or A * B) for one 256 x 128 x K product
+ * shared by the two CTAs of a cluster (tcgen05 cta_group::2, the 2-CTA MMA
+ * mode of "論文解説: FlashAttention-4 — Algorithm and Kernel Pipelining
+ * Co-Design for Asymmetric Hardware Scaling", Backwardパスの最適化): CTA r
+ * holds rows [128 r, 128 r + 128) of A and of C and the r-th half of B's N
+ * columns; CTA 0 issues the product.
+ *   A bf16 [256, K] row-major (K contiguous), K in {64, 128}.
+ *   mode bit 0 clear: B bf16 [128, K] row-major (both operands K-major);
+ *   mode bit 0 set:   B bf16 [K, 128] row-major, i.e. C = A * B with B N-major;
+ *   mode bit 1 set:   each CTA first copies its rows of A into tensor memory
+ *                     and the product reads them from there.
+ *   Valid modes: 0, 1, 2, 3.
+ *   C fp32 [256, 128] row-major (output).
+ * Device pointers, 16-byte aligned; returns FA_ERR_INVALID / FA_ERR_ALIGN
+ * before any launch for bad arguments.
+ */
+int fa_test_mma_pair(const void* A, const void* B, float* C, int K, int mode, fa_stream_t stream);
+
+/*
  * fa_test_mma_fp8 -- C = A8 * B8^T for one 128 x 128 x 128 tile with e4m3
  * operands (the products of the 8-bit forward path, fa_fwd_fp8).
  *   A, B fp32 [128, 128] row-major; each row is rounded to e4m3 on the

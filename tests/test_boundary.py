@@ -167,6 +167,10 @@ def test_testing_entry_point_argument_errors(lib):
     assert fa.fa_test_mma_tile(P, P, P, 64, 6, 0) == fa.FA_ERR_INVALID
     assert fa.fa_test_mma_tile(P, P, P, 64, -1, 0) == fa.FA_ERR_INVALID
     assert fa.fa_test_mma_tile(P + 8, P, P, 64, 0, 0) == fa.FA_ERR_ALIGN
+    assert fa.fa_test_mma_pair(P, P, P, 96, 0, 0) == fa.FA_ERR_INVALID
+    assert fa.fa_test_mma_pair(P, P, P, 64, 4, 0) == fa.FA_ERR_INVALID
+    assert fa.fa_test_mma_pair(P, P, P, 64, -1, 0) == fa.FA_ERR_INVALID
+    assert fa.fa_test_mma_pair(P, P + 8, P, 128, 0, 0) == fa.FA_ERR_ALIGN
     assert fa.fa_test_wait_timeout(5, 0) == fa.FA_ERR_INVALID
 
 

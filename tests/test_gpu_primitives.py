@@ -80,6 +80,27 @@ def test_mma_tile(torch, K, mode):
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-5
 
 
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_mma_pair(torch, K, mode):
+    """One 256 x 128 x K product shared by the two CTAs of a cluster
+    (cta_group::2): rows 0-127 of A and C in CTA 0, 128-255 in CTA 1, B's N
+    columns split between them; A from shared or tensor memory, B K- or
+    N-major."""
+    rng = np.random.default_rng(2000 + K + mode)
+    a_bits = fa_inputs_bits(rng, (256, K))
+    b_bits = fa_inputs_bits(rng, (K, 128) if mode & 1 else (128, K))
+    A, B = gu.dev_bf16(a_bits), gu.dev_bf16(b_bits)
+    C = torch.full((256, 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert fa.fa_test_mma_pair(A.data_ptr(), B.data_ptr(), C.data_ptr(), K, mode, 0) == fa.FA_OK
+    assert fa.fa_get_last_device_status(0) == fa.FA_OK
+    a = gu.fa_inputs.bf16_bits_to_f64(a_bits)
+    b = gu.fa_inputs.bf16_bits_to_f64(b_bits)
+    ref = a @ b if mode & 1 else a @ b.T
+    got = C.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-5
+
+
 def fa_inputs_bits(rng, shape):
     return gu.fa_inputs.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
 
